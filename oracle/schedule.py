@@ -1,0 +1,93 @@
+"""Integer work mapping of FlashAttention-2, as the pages describe it.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Forward ("FlashAttention学习笔记(2)" and "大猿搬砖简记", sections on the V2
+thread-block layout): one worker per (Q row block, batch, head); the number of
+row blocks is ceil(seqlen_q / kBlockM) and the grid is (num_m_block, batch,
+heads), with the row-block index varying fastest so that the workers that read
+the same K/V run close together (L2 reuse).
+
+Backward ("Foward和backward中的thread block划分" section of the first page, and
+the matching section of "大猿搬砖简记"): one worker per K/V column block, since
+dK and dV accumulate along the query direction and only dQ accumulates along
+the key direction.
+
+Causal tile skipping ("flash-attention123和ring-attention", 优化3): key/query
+tile pairs that the causal mask hides completely are dropped, not computed.
+Reading (the first two pages say such tiles are still loaded; the third says
+they are skipped): they are neither loaded nor computed. A tile pair is fully
+masked iff every key index in it exceeds every query index in it.
+"""
+
+from __future__ import annotations
+
+__all__ = [
+    "ceil_div",
+    "fwd_grid",
+    "fwd_work_order",
+    "fwd_kv_tile_range",
+    "bwd_grid",
+    "bwd_q_tile_range",
+]
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def fwd_grid(B: int, H: int, N: int, block_m: int):
+    """(num_m_block, B, H): the forward grid of the pages."""
+    return (ceil_div(N, block_m), B, H)
+
+
+def fwd_work_order(B: int, H: int, N: int, block_m: int):
+    """Linear order of forward workers: list of (m_block, b, h), m fastest."""
+    nm, _, _ = fwd_grid(B, H, N, block_m)
+    return [(m, b, h) for h in range(H) for b in range(B) for m in range(nm)]
+
+
+def _tile_fully_masked(q0, q1, k0, k1):
+    """Query rows [q0, q1) and key columns [k0, k1): fully hidden by the causal
+    mask iff the smallest key index exceeds the largest query index."""
+    return k0 > q1 - 1
+
+
+def fwd_kv_tile_range(m_block: int, N: int, block_m: int, block_n: int, causal: bool):
+    """Half-open range [j_begin, j_end) of K/V tiles a forward worker visits.
+
+    Derived by brute force over all tiles, dropping fully masked ones, so that
+    it is independent of any closed-form bound.
+    """
+    q0, q1 = m_block * block_m, min(N, (m_block + 1) * block_m)
+    visited = []
+    for j in range(ceil_div(N, block_n)):
+        k0, k1 = j * block_n, min(N, (j + 1) * block_n)
+        if causal and _tile_fully_masked(q0, q1, k0, k1):
+            continue
+        visited.append(j)
+    if not visited:
+        return (0, 0)
+    assert visited == list(range(visited[0], visited[-1] + 1))
+    return (visited[0], visited[-1] + 1)
+
+
+def bwd_grid(B: int, H: int, N: int, block_n: int):
+    """(num_n_block, B, H): one backward worker per K/V column block."""
+    return (ceil_div(N, block_n), B, H)
+
+
+def bwd_q_tile_range(n_block: int, N: int, block_m: int, block_n: int, causal: bool):
+    """Half-open range [i_begin, i_end) of Q tiles a backward column worker visits
+    (brute force over all tiles, dropping fully masked ones)."""
+    k0, k1 = n_block * block_n, min(N, (n_block + 1) * block_n)
+    visited = []
+    for i in range(ceil_div(N, block_m)):
+        q0, q1 = i * block_m, min(N, (i + 1) * block_m)
+        if causal and _tile_fully_masked(q0, q1, k0, k1):
+            continue
+        visited.append(i)
+    if not visited:
+        return (0, 0)
+    assert visited == list(range(visited[0], visited[-1] + 1))
+    return (visited[0], visited[-1] + 1)
