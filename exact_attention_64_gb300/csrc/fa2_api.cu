@@ -1,0 +1,322 @@
+// C ABI of libfa2.so: argument validation, TMA tensor maps, the device status
+// word and the kernel launches. Declarations and argument contracts live in
+// include/fa2.h.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/fa2.h"
+#include "fa2_common.cuh"
+
+namespace fa2 {
+cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
+                       cudaStream_t stream);
+cudaError_t launch_bwd(int d, bool bf16, bool causal, const void* o, const void* dO,
+                       const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
+                       float* l2, cudaStream_t stream, cudaEvent_t* ev);
+}  // namespace fa2
+
+namespace {
+
+// One status word per device: a static device variable, so the library makes
+// no allocation of its own.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+int g_arch_ok[kMaxDevices];        // 0 unknown, 1 sm_103, -1 other
+int* g_status_ptr[kMaxDevices];    // device address of g_device_status, per device
+int g_fault_kind = 0;              // armed by fa2_debug_arm_fault, consumed by the next fwd
+unsigned long long g_fault_timeout_ns = 0;
+
+int current_device(int* dev) {
+  return cudaGetDevice(dev) == cudaSuccess && *dev >= 0 && *dev < kMaxDevices ? FA2_OK
+                                                                               : FA2_ERR_CUDA;
+}
+
+// Per-device set-up: architecture check and the status word's device address.
+int device_setup(int* dev_out, int** status_out) {
+  int dev = 0;
+  if (current_device(&dev) != FA2_OK) return FA2_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA2_ERR_CUDA;
+    g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_arch_ok[dev] != 1) return FA2_ERR_ARCH;
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return FA2_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  if (g_encode == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return FA2_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  *dev_out = dev;
+  *status_out = g_status_ptr[dev];
+  return FA2_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int check_common(int B, int H, int N, int d, int causal, float scale, int dtype) {
+  if (B < 1 || H < 1 || N < 1) return FA2_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA2_ERR_INVALID_ARG;
+  if (dtype != FA2_FP16 && dtype != FA2_BF16) return FA2_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA2_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535) return FA2_ERR_UNSUPPORTED;
+  // Row indices of [B*H*N] stay within int32 (TMA coordinates and padded row
+  // offsets); element offsets are computed in 64 bits.
+  const long long rows = static_cast<long long>(B) * H * (N + 127);
+  if (rows > (1LL << 31) - 1) return FA2_ERR_UNSUPPORTED;
+  return FA2_OK;
+}
+
+// 3-D tensor map over a [B*H][N][d] 16-bit tensor, boxes of 128 rows x 64
+// columns (one 128-byte-swizzled slab), zero fill past row N of each head.
+int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dtype) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa2::kTileRows), 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r =
+      g_encode(m, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+               3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+             int d, int causal, float scale, int dtype, int* tile_counts, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, d, causal, scale, dtype);
+  if (st != FA2_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA2_ERR_ALIGNMENT;
+  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  const void* ins[3] = {q, k, v};
+  for (const void* in : ins)
+    if (overlap(o, tbytes, in, tbytes) || overlap(lse, lbytes, in, tbytes)) return FA2_ERR_OVERLAP;
+  if (overlap(o, tbytes, lse, lbytes)) return FA2_ERR_OVERLAP;
+  int dev = 0;
+  int* status = nullptr;
+  st = device_setup(&dev, &status);
+  if (st != FA2_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv, to;
+  if (make_map_16bit(&tq, q, BH, N, d, dtype) || make_map_16bit(&tk, k, BH, N, d, dtype) ||
+      make_map_16bit(&tv, v, BH, N, d, dtype) || make_map_16bit(&to, o, BH, N, d, dtype))
+    return FA2_ERR_CUDA;
+  fa2::FwdArgs a{};
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.num_m_blocks = fa2::fwd_num_m_blocks(N);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.tile_count = tile_counts;
+  a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
+  a.fault = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_fault_kind != 0) {
+      a.fault = g_fault_kind;
+      a.timeout_ns = g_fault_timeout_ns;
+      g_fault_kind = 0;
+    }
+  }
+  const cudaError_t e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
+                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+            int d, int causal, float scale, int dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, nullptr, stream);
+}
+
+int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, int causal, float scale, int dtype, int* tile_counts,
+                         void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, tile_counts, stream);
+}
+
+size_t fa2_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  // [D: B*H x N_pad fp32][L*log2e: B*H x N_pad fp32], N_pad = N rounded up to
+  // the 128-row tile of the backward kernels.
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t n_pad = align_up(static_cast<size_t>(N), 128);
+  return 2 * align_up(bh * n_pad * 4, 256);
+}
+
+int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                  void* const* phase_events, void* stream) {
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, d, causal, scale, dtype);
+  if (st != FA2_OK) return st;
+  const void* in16[5] = {q, k, v, o, dO};
+  void* out16[3] = {dq, dk, dv};
+  for (const void* p : in16)
+    if (!aligned(p, 16)) return FA2_ERR_ALIGNMENT;
+  for (void* p : out16)
+    if (!aligned(p, 16)) return FA2_ERR_ALIGNMENT;
+  if (!aligned(lse, 4)) return FA2_ERR_ALIGNMENT;
+  const size_t need = fa2_bwd_workspace_size(B, H, N, d);
+  if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA2_ERR_ALIGNMENT;
+  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  for (void* out : out16) {
+    for (const void* in : in16)
+      if (overlap(out, tbytes, in, tbytes)) return FA2_ERR_OVERLAP;
+    if (overlap(out, tbytes, lse, lbytes) || overlap(out, tbytes, workspace, need))
+      return FA2_ERR_OVERLAP;
+  }
+  if (overlap(dq, tbytes, dk, tbytes) || overlap(dq, tbytes, dv, tbytes) ||
+      overlap(dk, tbytes, dv, tbytes))
+    return FA2_ERR_OVERLAP;
+  for (const void* in : in16)
+    if (overlap(workspace, need, in, tbytes)) return FA2_ERR_OVERLAP;
+  if (overlap(workspace, need, lse, lbytes)) return FA2_ERR_OVERLAP;
+  int dev = 0;
+  int* status = nullptr;
+  st = device_setup(&dev, &status);
+  if (st != FA2_OK) return st;
+  const int BH = B * H;
+  // Tensor maps: q, k, v, dO (loads), dk, dv, dq (stores); all 128-row boxes.
+  CUtensorMap maps[7];
+  const void* src[7] = {q, k, v, dO, dk, dv, dq};
+  for (int i = 0; i < 7; ++i)
+    if (make_map_16bit(&maps[i], src[i], BH, N, d, dtype) != FA2_OK) return FA2_ERR_CUDA;
+  const size_t n_pad = align_up(static_cast<size_t>(N), 128);
+  const size_t lbytes_pad = align_up(static_cast<size_t>(BH) * n_pad * 4, 256);
+  float* dsum = static_cast<float*>(workspace);
+  float* l2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + lbytes_pad);
+  fa2::BwdArgs a{};
+  a.l2_pad = l2;
+  a.dsum_pad = dsum;
+  a.n_pad = static_cast<int>(n_pad);
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
+  const cudaError_t e = fa2::launch_bwd(
+      d, dtype == FA2_BF16, causal != 0, o, dO, lse, maps, a, dsum, l2,
+      static_cast<cudaStream_t>(stream),
+      reinterpret_cast<cudaEvent_t*>(const_cast<void**>(phase_events)));
+  return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+}
+
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+            const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+            float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa2_bwd_timed(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, d, causal, scale, dtype,
+                       workspace, workspace_bytes, nullptr, stream);
+}
+
+int fa2_get_device_status(void* stream) {
+  int dev = 0;
+  int* status = nullptr;
+  const int st = device_setup(&dev, &status);
+  if (st != FA2_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA2_ERR_CUDA;
+  if (h != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return FA2_ERR_CUDA;
+  }
+  return h == 0 ? FA2_OK : h;
+}
+
+const char* fa2_status_string(int status) {
+  switch (status) {
+    case FA2_OK: return "FA2_OK";
+    case FA2_ERR_INVALID_ARG: return "FA2_ERR_INVALID_ARG";
+    case FA2_ERR_UNSUPPORTED: return "FA2_ERR_UNSUPPORTED";
+    case FA2_ERR_ALIGNMENT: return "FA2_ERR_ALIGNMENT";
+    case FA2_ERR_ARCH: return "FA2_ERR_ARCH";
+    case FA2_ERR_CUDA: return "FA2_ERR_CUDA";
+    case FA2_ERR_DEVICE_TIMEOUT: return "FA2_ERR_DEVICE_TIMEOUT";
+    case FA2_ERR_WORKSPACE: return "FA2_ERR_WORKSPACE";
+    case FA2_ERR_OVERLAP: return "FA2_ERR_OVERLAP";
+    default: return "FA2_ERR_UNKNOWN";
+  }
+}
+
+int fa2_fwd_grid(int B, int H, int N, int grid_out[3], int* rows_per_cta) {
+  if (B < 1 || H < 1 || N < 1 || grid_out == nullptr) return FA2_ERR_INVALID_ARG;
+  grid_out[0] = fa2::fwd_num_m_blocks(N);
+  grid_out[1] = B;
+  grid_out[2] = H;
+  if (rows_per_cta) *rows_per_cta = fa2::kFwdRowsPerCta;
+  return FA2_OK;
+}
+
+int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_end,
+                       int* kv_tiles) {
+  const int nm = N >= 1 ? fa2::fwd_num_m_blocks(N) : 0;
+  if (N < 1 || block_x < 0 || block_x >= nm || (causal != 0 && causal != 1))
+    return FA2_ERR_INVALID_ARG;
+  const int mb = fa2::fwd_m_block_of(block_x, nm, causal);
+  const int r0 = mb * fa2::kFwdRowsPerCta;
+  const int r1 = r0 + fa2::kFwdRowsPerCta < N ? r0 + fa2::kFwdRowsPerCta : N;
+  if (row_begin) *row_begin = r0;
+  if (row_end) *row_end = r1;
+  if (kv_tiles) *kv_tiles = fa2::fwd_kv_tile_end(r0, r1, N, causal);
+  return FA2_OK;
+}
+
+int fa2_debug_arm_fault(int kind, int timeout_ms) {
+  if (kind != 0 && kind != 1) return FA2_ERR_INVALID_ARG;
+  if (kind == 1 && (timeout_ms < 1 || timeout_ms > 5000)) return FA2_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_fault_kind = kind;
+  g_fault_timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;
+  return FA2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,667 @@
+// FlashAttention-2 backward for sm_103a: three kernels on one stream.
+//
+//  1. fa2_bwd_pre_kernel  D_i = sum_c dO[i][c] * O[i][c] in fp32 from the stored
+//                         O, and L_i * log2(e). The D shortcut stands in for
+//                         rowsum(P o dP) ("大猿搬砖简记", V2 backward, last
+//                         paragraph).
+//  2. fa2_bwd_dkdv_kernel K/V outer, Q inner ("FlashAttention学习笔记(2)",
+//                         Foward和backward中的thread block划分; "大猿搬砖简记",
+//                         V2 backward): one CTA per 128-key column block keeps
+//                         K_j, V_j in shared memory and dK_j, dV_j in TMEM while
+//                         128-row query tiles stream past; S and P are
+//                         recomputed from L ("flash-attention123和ring-attention",
+//                         优化1).
+//  3. fa2_bwd_dq_kernel   dQ, which accumulates along the key direction (the
+//                         "awkward" gradient of the V2 backward), gets a worker
+//                         of its own that owns a 128-row query tile and
+//                         accumulates dQ in fp32 TMEM over the visible K/V
+//                         tiles, recomputing S, dP and dS. This is the split
+//                         variant: no atomics, and dQ is bit-reproducible.
+//
+// Products (tcgen05, 16-bit operands, fp32 accumulate in TMEM):
+//   dK/dV kernel, per query tile i:  S^T = K Q_i^T, dP^T = V dO_i^T   (SS, M=128 keys, N=128 queries)
+//                                    dV += P^T dO_i, dK += dS^T Q_i   (TS, A from TMEM, M=128 keys, N=d)
+//   dQ kernel, per K/V tile j:       S = Q K_j^T, dP = dO V_j^T        (SS, M=128 queries, N=128 keys)
+//                                    dQ += dS K_j                      (TS, A from TMEM, M=128 queries, N=d)
+// with P = exp2(S * scale*log2e - L*log2e) and dS = P o (dP - D).
+#include <cuda_fp16.h>
+#include "fa2_common.cuh"
+#include "../../include/fa2.h"
+
+namespace fa2 {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int SLAB_BYTES = kTileRows * 128;    // 128 rows x 128 bytes
+  static constexpr int TILE_BYTES = kTileRows * D * 2;  // one 128-row Q, K, V or dO tile
+  static constexpr int NS = 2;                          // ring depth of the streamed pair
+  static constexpr int OFF_FIX0 = 0;                    // resident pair (K,V) or (Q,dO)
+  static constexpr int OFF_FIX1 = TILE_BYTES;
+  static constexpr int OFF_STR0 = 2 * TILE_BYTES;       // streamed pair, NS stages each
+  static constexpr int OFF_STR1 = OFF_STR0 + NS * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_STR1 + NS * TILE_BYTES;
+  // >= 116 KiB so that at most one CTA (one 512-column TMEM allocation) lives on an SM.
+  static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 118784) ? SMEM_BYTES + 1024 : 118784;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t TMEM_COLS = 512;
+  // dK/dV kernel TMEM: dV, dK accumulators, S^T and dP^T (P^T / dS^T overwrite
+  // the first 32 columns of each warpgroup's 64-column half).
+  static constexpr uint32_t KV_DV = 0, KV_DK = D, KV_ST = 2 * D, KV_DPT = 2 * D + 128;
+  // dQ kernel TMEM: S, dP, the dQ accumulator and two dS buffers.
+  static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256;
+  __host__ __device__ static constexpr uint32_t Q_DS(int b) { return 256 + D + 64 * b; }
+};
+
+struct BwdKvShared {
+  uint64_t kv_full;
+  uint64_t s_full[2], s_empty[2];  // streamed pair ring (Q_i, dO_i)
+  uint64_t st_full, sm_done, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BwdQShared {
+  uint64_t q_full;
+  uint64_t s_full[2], s_empty[2];  // streamed pair ring (K_j, V_j)
+  uint64_t st_full, s_free, ds_full, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// ---------------------------------------------------------------------------
+// 1. preprocess
+// ---------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa2_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                       const float* __restrict__ lse, float* __restrict__ dsum_pad,
+                       float* __restrict__ l2_pad, int BH, int N, int n_pad) {
+  constexpr int EPL = D / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
+  const int lane = threadIdx.x & 31;
+  const long long total = static_cast<long long>(BH) * n_pad;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total; r += warps) {
+    const int bh = static_cast<int>(r / n_pad), i = static_cast<int>(r % n_pad);
+    float dsum = 0.f, l2 = 0.f;
+    if (i < N) {
+      const size_t row = static_cast<size_t>(bh) * N + i;
+      const uint16_t* po = o + row * D + lane * EPL;
+      const uint16_t* pd = dout + row * D + lane * EPL;
+      uint32_t ow[EPL / 2], dw[EPL / 2];
+      if constexpr (EPL == 4) {
+        const uint2 x = *reinterpret_cast<const uint2*>(po);
+        const uint2 y = *reinterpret_cast<const uint2*>(pd);
+        ow[0] = x.x; ow[1] = x.y; dw[0] = y.x; dw[1] = y.y;
+      } else {
+        ow[0] = *reinterpret_cast<const uint32_t*>(po);
+        dw[0] = *reinterpret_cast<const uint32_t*>(pd);
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < EPL / 2; ++w) {
+        float o0, o1, d0, d1;
+        if constexpr (BF16) {
+          o0 = __uint_as_float(ow[w] << 16); o1 = __uint_as_float(ow[w] & 0xffff0000u);
+          d0 = __uint_as_float(dw[w] << 16); d1 = __uint_as_float(dw[w] & 0xffff0000u);
+        } else {
+          const __half2 oh = *reinterpret_cast<const __half2*>(&ow[w]);
+          const __half2 dh = *reinterpret_cast<const __half2*>(&dw[w]);
+          o0 = __low2float(oh); o1 = __high2float(oh);
+          d0 = __low2float(dh); d1 = __high2float(dh);
+        }
+        acc = fmaf(o0, d0, acc);
+        acc = fmaf(o1, d1, acc);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      dsum = acc;
+      l2 = lse[row] * kLog2e;
+    }
+    if (lane == 0) {
+      dsum_pad[r] = dsum;
+      l2_pad[r] = l2;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Shared pieces of the two tensor-core kernels
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                          int row, int bh) {
+#pragma unroll
+  for (int s = 0; s < D / 64; ++s)
+    tma_load_3d(dst + s * BwdCfg<D>::SLAB_BYTES, map, bar, s * 64, row, bh);
+}
+
+// D[tmem] = A B^T over the head dimension: M=128 rows of A, N=128 rows of B,
+// K=d. Both tiles K-major, 128-byte swizzled (the forward's Q K^T form).
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  constexpr uint32_t idesc = make_idesc_f16(128, 128, BF16, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * BwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
+    umma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024),
+            make_sdesc_sw128(b_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// D[tmem] (+)= A[tmem] X with A = 128 x 128 16-bit pairs in TMEM and X a
+// 128-row tile [row][d] in shared memory (MN-major for this product; the
+// forward's P V form). a_col(kk) gives the TMEM column of A's 16-row block kk.
+template <int D, bool BF16, typename ACol>
+__device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uint32_t x_smem,
+                                                bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
+#pragma unroll
+  for (int kk = 0; kk < kTileRows / 16; ++kk)
+    umma_ts(d_tmem, a_col(kk), make_sdesc_sw128(x_smem + kk * 2048, BwdCfg<D>::SLAB_BYTES, 1024),
+            idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Stage a 128 x d fp32 TMEM accumulator (this thread's lane = row r) as 16-bit
+// rows, multiplied by mul, into a 128-byte-swizzled tile in shared memory.
+template <int D, bool BF16>
+__device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r, float mul) {
+#pragma unroll
+  for (int c = 0; c < D; c += 32) {
+    uint32_t x[32];
+    tmem_ld_32x32b_x32(t_src + c, x);
+    tmem_wait_ld();
+    reg_fence(x);
+    const int slab = c / 64, chunk0 = (c % 64) / 8;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 val;
+      val.x = pack_x2<BF16>(__uint_as_float(x[8 * k + 0]) * mul, __uint_as_float(x[8 * k + 1]) * mul);
+      val.y = pack_x2<BF16>(__uint_as_float(x[8 * k + 2]) * mul, __uint_as_float(x[8 * k + 3]) * mul);
+      val.z = pack_x2<BF16>(__uint_as_float(x[8 * k + 4]) * mul, __uint_as_float(x[8 * k + 5]) * mul);
+      val.w = pack_x2<BF16>(__uint_as_float(x[8 * k + 6]) * mul, __uint_as_float(x[8 * k + 7]) * mul);
+      *reinterpret_cast<uint4*>(stage + slab * BwdCfg<D>::SLAB_BYTES + r * 128 +
+                                (((chunk0 + k) ^ (r & 7)) * 16)) = val;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. dK / dV kernel (K/V outer, Q inner)
+// ---------------------------------------------------------------------------
+// Warp roles: warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 compute P^T and dS^T
+// for query columns [0,64) and [64,128) of each tile (TMEM lane = key).
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                        const BwdArgs a) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ BwdKvShared sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int nb = blockIdx.x;                     // key block, fastest grid axis
+  const int bh = blockIdx.y * a.H + blockIdx.z;  // grid = (n block, batch, head)
+  const int n0 = nb * kTileRows;
+  const int i_begin = bwd_q_tile_begin(nb, CAUSAL);
+  const int n_steps = ceil_div(N, kTileRows) - i_begin;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
+    mbar_init(&sh.st_full, 1);
+    mbar_init(&sh.sm_done, 8);
+    mbar_init(&sh.mma_done, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort_flag;
+  const WaitCtx wc{a.status, abort_flag, a.timeout_ns};
+
+  if (warp < 4) {
+    setmaxnreg_dec<64>();
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
+      load_tile<D>(smem + C::OFF_FIX0, &tm_k, &sh.kv_full, n0, bh);
+      load_tile<D>(smem + C::OFF_FIX1, &tm_v, &sh.kv_full, n0, bh);
+      int i = 0;
+      bool ok = true;
+      for (; i < n_steps; ++i) {
+        const int st = i % C::NS, ph = (i / C::NS) & 1;
+        ok = mbar_wait(&sh.s_empty[st], ph ^ 1, wc);
+        if (!ok) break;
+        const int q0 = (i_begin + i) * kTileRows;
+        mbar_arrive_expect_tx(&sh.s_full[st], 2 * C::TILE_BYTES);
+        load_tile<D>(smem + C::OFF_STR0 + st * C::TILE_BYTES, &tm_q, &sh.s_full[st], q0, bh);
+        load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_do, &sh.s_full[st], q0, bh);
+      }
+      if (!ok) {
+        mbar_wait_drain(&sh.kv_full, 0, a.timeout_ns);
+        for (int ii = max(0, i - C::NS); ii < i; ++ii)
+          mbar_wait_drain(&sh.s_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- tcgen05.mma issuer ----------------
+      const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
+      bool ok = mbar_wait(&sh.kv_full, 0, wc) && mbar_wait(&sh.s_full[0], 0, wc);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, smem_u32(smem + C::OFF_STR0));
+        mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, smem_u32(smem + C::OFF_STR1));
+        umma_commit(&sh.st_full);
+      }
+      for (int i = 0; i < n_steps && ok; ++i) {
+        const int st = i % C::NS;
+        ok = mbar_wait(&sh.sm_done, i & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
+        const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
+        // P^T / dS^T of query block kk (16 queries) live in the first 32 columns
+        // of the 64-column half that holds that block.
+        const uint32_t pt_base = tmem + C::KV_ST, dst_base = tmem + C::KV_DPT;
+        mma_tmem_x_tile<D, BF16>(
+            tmem + C::KV_DV, [pt_base](int kk) { return pt_base + 64u * (kk / 4) + 8u * (kk % 4); },
+            do_s, i > 0);
+        mma_tmem_x_tile<D, BF16>(
+            tmem + C::KV_DK, [dst_base](int kk) { return dst_base + 64u * (kk / 4) + 8u * (kk % 4); },
+            q_s, i > 0);
+        umma_commit(&sh.s_empty[st]);
+        if (i + 1 < n_steps) {
+          const int sn = (i + 1) % C::NS;
+          ok = mbar_wait(&sh.s_full[sn], ((i + 1) / C::NS) & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, smem_u32(smem + C::OFF_STR0 + sn * C::TILE_BYTES));
+          mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, smem_u32(smem + C::OFF_STR1 + sn * C::TILE_BYTES));
+          umma_commit(&sh.st_full);
+        }
+      }
+      umma_commit(&sh.mma_done);
+      mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
+    }
+  } else {
+    setmaxnreg_inc<208>();
+    // ---------------- P^T / dS^T warpgroups ----------------
+    const int wg = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // key row of the block == TMEM lane
+    const int kg = n0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t t_st = tmem + lane_off + C::KV_ST + 64 * wg;
+    const uint32_t t_dpt = tmem + lane_off + C::KV_DPT + 64 * wg;
+    const float sl2 = a.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n_steps; ++i) {
+      const int q0 = (i_begin + i) * kTileRows;
+      const int qc0 = q0 + 64 * wg;  // first query column of this warpgroup
+      ok = mbar_wait(&sh.st_full, i & 1, wc);
+      if (!ok) break;
+      __syncwarp();  // the warp-collective TMEM loads below need a converged warp
+      tc_fence_after();
+      const bool need_mask = (CAUSAL && qc0 < n0 + kTileRows - 1) || (qc0 + 64 > N) ||
+                             (n0 + kTileRows > N);
+      const float4* pl = reinterpret_cast<const float4*>(a.l2_pad + static_cast<size_t>(bh) * a.n_pad + qc0);
+      const float4* pd = reinterpret_cast<const float4*>(a.dsum_pad + static_cast<size_t>(bh) * a.n_pad + qc0);
+      uint32_t pp[32], dsp[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t s[32], dp[32];
+        tmem_ld_32x32b_x32(t_st + 32 * h, s);
+        tmem_ld_32x32b_x32(t_dpt + 32 * h, dp);
+        tmem_wait_ld();
+        reg_fence(s);
+        reg_fence(dp);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 l4 = __ldg(pl + 8 * h + u), d4 = __ldg(pd + 8 * h + u);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * u + e;
+            p[e] = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -lv[e]));
+            if (need_mask) {
+              const int qq = qc0 + 32 * h + c;
+              if (kg >= N || qq >= N || (CAUSAL && kg > qq)) p[e] = 0.f;
+            }
+            ds[e] = p[e] * (__uint_as_float(dp[c]) - dv[e]);
+          }
+          pp[16 * h + 2 * u] = pack_x2<BF16>(p[0], p[1]);
+          pp[16 * h + 2 * u + 1] = pack_x2<BF16>(p[2], p[3]);
+          dsp[16 * h + 2 * u] = pack_x2<BF16>(ds[0], ds[1]);
+          dsp[16 * h + 2 * u + 1] = pack_x2<BF16>(ds[2], ds[3]);
+        }
+      }
+      // Both 32-column halves have been read: overwrite the first 32 columns.
+      tmem_st_32x32b_x32(t_st, pp);
+      tmem_st_32x32b_x32(t_dpt, dsp);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.sm_done);
+    }
+    // ---------------- epilogue: dV, scale*dK -> 16-bit, TMA store ----------------
+    if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
+    // All MMAs have completed, so the K and V buffers are free for staging.
+    uint8_t* stage = smem + (wg == 0 ? C::OFF_FIX1 : C::OFF_FIX0);
+    if (ok) {
+      __syncwarp();
+      tc_fence_after();
+      stage_rows<D, BF16>(stage, tmem + lane_off + (wg == 0 ? C::KV_DV : C::KV_DK), r,
+                          wg == 0 ? 1.f : a.scale);
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + wg, 128);
+    if ((threadIdx.x & 127) == 0 && *abort_flag == 0) {
+      const CUtensorMap* map = (wg == 0) ? &tm_dv : &tm_dk;
+#pragma unroll
+      for (int s = 0; s < D / 64; ++s) tma_store_3d(map, stage + s * C::SLAB_BYTES, s * 64, n0, bh);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dQ kernel (Q outer, K/V inner)
+// ---------------------------------------------------------------------------
+// Warp roles: warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 compute dS for key
+// columns [0,64) and [64,128) of each K/V tile (TMEM lane = query row).
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa2_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a, int num_m_blocks) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ BwdQShared sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int mb = dq_m_block_of(blockIdx.x, num_m_blocks, CAUSAL);
+  const int bh = blockIdx.y * a.H + blockIdx.z;
+  const int q0 = mb * kTileRows;
+  const int n_kv = fwd_kv_tile_end(q0, min(N, q0 + kTileRows), N, CAUSAL);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.q_full, 1);
+    for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
+    mbar_init(&sh.st_full, 1);
+    mbar_init(&sh.s_free, 8);
+    mbar_init(&sh.ds_full, 8);
+    mbar_init(&sh.mma_done, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort_flag;
+  const WaitCtx wc{a.status, abort_flag, a.timeout_ns};
+
+  if (warp < 4) {
+    setmaxnreg_dec<64>();
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&sh.q_full, 2 * C::TILE_BYTES);
+      load_tile<D>(smem + C::OFF_FIX0, &tm_q, &sh.q_full, q0, bh);
+      load_tile<D>(smem + C::OFF_FIX1, &tm_do, &sh.q_full, q0, bh);
+      int j = 0;
+      bool ok = true;
+      for (; j < n_kv; ++j) {
+        const int st = j % C::NS, ph = (j / C::NS) & 1;
+        ok = mbar_wait(&sh.s_empty[st], ph ^ 1, wc);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sh.s_full[st], 2 * C::TILE_BYTES);
+        load_tile<D>(smem + C::OFF_STR0 + st * C::TILE_BYTES, &tm_k, &sh.s_full[st], j * kTileRows, bh);
+        load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_v, &sh.s_full[st], j * kTileRows, bh);
+      }
+      if (!ok) {
+        mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
+        for (int jj = max(0, j - C::NS); jj < j; ++jj)
+          mbar_wait_drain(&sh.s_full[jj % C::NS], (jj / C::NS) & 1, a.timeout_ns);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- tcgen05.mma issuer ----------------
+      const uint32_t q_s = smem_u32(smem + C::OFF_FIX0), do_s = smem_u32(smem + C::OFF_FIX1);
+      bool ok = mbar_wait(&sh.q_full, 0, wc) && mbar_wait(&sh.s_full[0], 0, wc);
+      if (ok) {
+        tc_fence_after();
+        mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, smem_u32(smem + C::OFF_STR0));
+        mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, smem_u32(smem + C::OFF_STR1));
+        umma_commit(&sh.st_full);
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int st = j % C::NS, b = j & 1;
+        // S(j), dP(j) have been read into registers: issue the next pair at once.
+        ok = mbar_wait(&sh.s_free, j & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        if (j + 1 < n_kv) {
+          const int sn = (j + 1) % C::NS;
+          ok = mbar_wait(&sh.s_full[sn], ((j + 1) / C::NS) & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, smem_u32(smem + C::OFF_STR0 + sn * C::TILE_BYTES));
+          mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, smem_u32(smem + C::OFF_STR1 + sn * C::TILE_BYTES));
+          umma_commit(&sh.st_full);
+        }
+        ok = mbar_wait(&sh.ds_full, j & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ds_col = tmem + C::Q_DS(b);
+        mma_tmem_x_tile<D, BF16>(tmem + C::Q_DQ, [ds_col](int kk) { return ds_col + 8u * kk; },
+                                 smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES), j > 0);
+        umma_commit(&sh.s_empty[st]);
+      }
+      umma_commit(&sh.mma_done);
+      mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
+    }
+  } else {
+    setmaxnreg_inc<208>();
+    // ---------------- dS warpgroups ----------------
+    const int wg = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // query row of the tile == TMEM lane
+    const int my_row = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = a.scale_log2;
+    const float l2 = a.l2_pad[static_cast<size_t>(bh) * a.n_pad + my_row];
+    const float dsum = a.dsum_pad[static_cast<size_t>(bh) * a.n_pad + my_row];
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int b = j & 1;
+      const int kc0 = j * kTileRows + 64 * wg;  // first key column of this warpgroup
+      ok = mbar_wait(&sh.st_full, j & 1, wc);
+      if (!ok) break;
+      __syncwarp();  // the warp-collective TMEM loads below need a converged warp
+      tc_fence_after();
+      uint32_t s[64], dp[64];
+      tmem_ld_32x32b_x32(tmem + lane_off + C::Q_S + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld_32x32b_x32(tmem + lane_off + C::Q_S + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld_32x32b_x32(tmem + lane_off + C::Q_DP + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+      tmem_ld_32x32b_x32(tmem + lane_off + C::Q_DP + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      tmem_wait_ld();
+      reg_fence(s);
+      reg_fence(dp);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.s_free);
+      const bool need_mask = (CAUSAL && kc0 + 63 > q0) || (kc0 + 64 > N) || (q0 + kTileRows > N);
+      const int lim = CAUSAL ? min(N, my_row + 1) : N;  // keys < lim are visible
+      const bool row_ok = my_row < N;
+      uint32_t dsp[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -l2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -l2));
+        if (need_mask) {
+          if (!row_ok || kc0 + c >= lim) p0 = 0.f;
+          if (!row_ok || kc0 + c + 1 >= lim) p1 = 0.f;
+        }
+        dsp[c / 2] = pack_x2<BF16>(p0 * (__uint_as_float(dp[c]) - dsum),
+                                   p1 * (__uint_as_float(dp[c + 1]) - dsum));
+      }
+      tmem_st_32x32b_x32(tmem + lane_off + C::Q_DS(b) + 32 * wg, dsp);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.ds_full);
+    }
+    // ---------------- epilogue: scale * dQ -> 16-bit, TMA store ----------------
+    if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
+    // Every MMA has completed: the Q buffer is free for staging.
+    uint8_t* stage = smem + C::OFF_FIX0;
+    if (ok && wg == 0) {
+      __syncwarp();
+      tc_fence_after();
+      stage_rows<D, BF16>(stage, tmem + lane_off + C::Q_DQ, r, a.scale);
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + wg, 128);
+    if (wg == 0 && (threadIdx.x & 127) == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int s = 0; s < D / 64; ++s) tma_store_3d(&tm_dq, stage + s * C::SLAB_BYTES, s * 64, q0, bh);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launcher
+// ---------------------------------------------------------------------------
+static int g_num_sms = 0;
+
+template <int D, bool BF16, bool CAUSAL>
+static cudaError_t launch_bwd_t(const void* o, const void* dO, const float* lse,
+                                const CUtensorMap* maps, const BwdArgs& a, float* dsum,
+                                float* l2, cudaStream_t stream, cudaEvent_t* ev) {
+  using C = BwdCfg<D>;
+  const int BH = a.B * a.H;
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 148;
+  }
+  if (ev) cudaEventRecord(ev[0], stream);
+  {
+    const long long rows = static_cast<long long>(BH) * a.n_pad;
+    long long blocks = (rows + 7) / 8;
+    const long long cap = static_cast<long long>(g_num_sms) * 16;
+    if (blocks > cap) blocks = cap;
+    fa2_bwd_pre_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, dsum, l2, BH,
+        a.N, a.n_pad);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (ev) cudaEventRecord(ev[1], stream);
+  {
+    auto kern = fa2_bwd_dkdv_kernel<D, BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    dim3 grid(bwd_num_n_blocks(a.N), a.B, a.H);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                      maps[5], a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (ev) cudaEventRecord(ev[2], stream);
+  {
+    auto kern = fa2_bwd_dq_kernel<D, BF16, CAUSAL>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e != cudaSuccess) return e;
+    const int nm = dq_num_m_blocks(a.N);
+    dim3 grid(nm, a.B, a.H);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[6],
+                                                      a, nm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (ev) cudaEventRecord(ev[3], stream);
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd(int d, bool bf16, bool causal, const void* o, const void* dO,
+                       const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
+                       float* l2, cudaStream_t stream, cudaEvent_t* ev) {
+#define FA2_BWD_CASE(DD, BB, CC) \
+  if (d == DD && bf16 == BB && causal == CC) \
+    return launch_bwd_t<DD, BB, CC>(o, dO, lse, maps, a, dsum, l2, stream, ev);
+  FA2_BWD_CASE(64, true, false)
+  FA2_BWD_CASE(64, true, true)
+  FA2_BWD_CASE(64, false, false)
+  FA2_BWD_CASE(64, false, true)
+  FA2_BWD_CASE(128, true, false)
+  FA2_BWD_CASE(128, true, true)
+  FA2_BWD_CASE(128, false, false)
+  FA2_BWD_CASE(128, false, true)
+#undef FA2_BWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa2
+
+extern "C" int fa2_bwd_grid(int B, int H, int N, int d, int grid_out[3], int* keys_per_cta,
+                            int* q_rows_per_tile) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || !grid_out) return FA2_ERR_INVALID_ARG;
+  grid_out[0] = fa2::bwd_num_n_blocks(N);
+  grid_out[1] = B;
+  grid_out[2] = H;
+  if (keys_per_cta) *keys_per_cta = fa2::kTileRows;
+  if (q_rows_per_tile) *q_rows_per_tile = fa2::kTileRows;
+  return FA2_OK;
+}
+
+extern "C" int fa2_bwd_block_work(int block_x, int N, int d, int causal, int* key_begin,
+                                  int* key_end, int* q_tile_begin, int* q_tile_end) {
+  if (N < 1 || (d != 64 && d != 128) || block_x < 0 || block_x >= fa2::bwd_num_n_blocks(N) ||
+      (causal != 0 && causal != 1))
+    return FA2_ERR_INVALID_ARG;
+  const int k0 = block_x * fa2::kTileRows;
+  if (key_begin) *key_begin = k0;
+  if (key_end) *key_end = (k0 + fa2::kTileRows < N) ? k0 + fa2::kTileRows : N;
+  if (q_tile_begin) *q_tile_begin = fa2::bwd_q_tile_begin(block_x, causal);
+  if (q_tile_end) *q_tile_end = fa2::ceil_div(N, fa2::kTileRows);
+  return FA2_OK;
+}

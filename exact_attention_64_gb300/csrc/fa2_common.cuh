@@ -1,0 +1,100 @@
+// Shared definitions of the FlashAttention-2 library: argument blocks, the
+// work mapping (which rows/keys each CTA owns) and small device utilities.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "sm103_ptx.cuh"
+
+namespace fa2 {
+
+__host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Q, K, V row tiles are 128 rows: one tcgen05 M=128 MMA covers one tile and
+// TMEM lane i holds row i of it.
+constexpr int kTileRows = 128;
+// A forward CTA owns two adjacent Q tiles (256 query rows) of one (batch, head)
+// and streams every visible K/V tile once for both of them.
+constexpr int kFwdRowsPerCta = 2 * kTileRows;
+
+// Forward work mapping. The grid is (num_m_block, batch, heads) with the row
+// block varying fastest, as in the FlashAttention-2 thread-block layout
+// ("FlashAttention学习笔记(2)", V2中的thread blocks排布): CTAs that read the same
+// K/V run back to back and share it through L2. Under a causal mask the row
+// blocks are launched longest first.
+__host__ __device__ inline int fwd_num_m_blocks(int N) { return ceil_div(N, kFwdRowsPerCta); }
+
+__host__ __device__ inline int fwd_m_block_of(int block_x, int num_m_blocks, int causal) {
+  return causal ? (num_m_blocks - 1 - block_x) : block_x;
+}
+
+// Half-open K/V tile range [0, end) that query rows [row_begin, row_end) visit.
+// Under the causal mask a K/V tile whose first key is past the last query row
+// is entirely masked and is skipped, neither loaded nor computed
+// ("flash-attention123和ring-attention", 优化3).
+__host__ __device__ inline int fwd_kv_tile_end(int row_begin, int row_end, int N, int causal) {
+  if (row_end <= row_begin) return 0;
+  return causal ? ceil_div(row_end, kTileRows) : ceil_div(N, kTileRows);
+}
+
+// Backward work mapping. dK and dV accumulate along the query direction, so
+// their worker owns a K/V column block ("FlashAttention学习笔记(2)",
+// Foward和backward中的thread block划分): one CTA per 128-key block, the column
+// block varying fastest, visiting 128-row query tiles from the first one that
+// reaches the diagonal. dQ accumulates along the key direction; its worker owns
+// a 128-row query tile and visits the K/V tiles up to the diagonal, like the
+// forward (causal: longest first).
+__host__ __device__ inline int bwd_num_n_blocks(int N) { return ceil_div(N, kTileRows); }
+
+__host__ __device__ inline int bwd_q_tile_begin(int n_block, int causal) {
+  return causal ? n_block : 0;
+}
+
+__host__ __device__ inline int dq_num_m_blocks(int N) { return ceil_div(N, kTileRows); }
+
+__host__ __device__ inline int dq_m_block_of(int block_x, int num_m_blocks, int causal) {
+  return causal ? (num_m_blocks - 1 - block_x) : block_x;
+}
+
+// Argument block of the forward kernel (tensor maps travel separately as
+// __grid_constant__ parameters).
+struct FwdArgs {
+  float* lse;         // [B*H, N] fp32, natural-log logsumexp
+  int B, H, N;
+  int num_m_blocks;   // ceil(N / 256)
+  float scale_log2;   // scale * log2(e)
+  int* status;        // device status word
+  int* tile_count;    // optional: per-CTA count of K/V tiles loaded (nullptr = off)
+  unsigned long long timeout_ns;  // bound on every mbarrier wait
+  int fault;          // 0 normally; 1 = producer skips the first V tile (failure-path test)
+};
+
+struct BwdArgs {
+  const float* l2_pad;    // L * log2(e), [B*H, n_pad] fp32 (0 past row N)
+  const float* dsum_pad;  // D = rowsum(dO o O), [B*H, n_pad] fp32 (0 past row N)
+  int n_pad;              // N rounded up to 128
+  int B, H, N;
+  float scale;            // softmax scale
+  float scale_log2;       // scale * log2(e)
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+}  // namespace fa2

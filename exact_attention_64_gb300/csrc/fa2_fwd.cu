@@ -1,0 +1,405 @@
+// FlashAttention-2 forward for sm_103a (tcgen05 + TMA + TMEM).
+//
+// What it computes (per (batch, head), rows independent):
+//   S = scale * Q K^T, causal mask j > i -> -inf,
+//   O = softmax(S) V,   L = m + ln(l)  (logsumexp, the only statistic stored).
+// The loop order is the FlashAttention-2 one: Q is the outer loop (each CTA
+// owns query rows), K/V is the inner loop streamed through shared memory, and
+// nothing but O and L ever leaves the chip ("FlashAttention学习笔记(2)", opening
+// section; "flash-attention123和ring-attention", 优化1). The online softmax keeps
+// a running row max m and row sum l; O accumulates un-normalised and is divided
+// by l once at the end ("flash-attention123和ring-attention", 优化2). K/V tiles
+// that the causal mask hides completely are skipped, not loaded (优化3).
+//
+// GB300 mapping (one CTA = two 128-row Q tiles "A" and "B" of one head):
+//   warp 0        TMA producer: Q_A, Q_B once, then K_j, V_j through
+//                 multi-stage shared-memory rings (mbarrier full/empty pairs).
+//   warp 1        tcgen05.mma issuer (one thread): S_t = Q_t K_j^T into TMEM,
+//                 O_t += P_t V_j with P_t read straight from TMEM.
+//   warps 4-7     softmax of tile A, warps 8-11 softmax of tile B. TMEM lane i
+//                 is query row i, so one thread owns one whole row: the row max
+//                 and row sum need no shuffles. The two tiles ping-pong, so the
+//                 tensor core works on one tile while the other's exponentials
+//                 run.
+// TMEM (512 columns): S_A [0,128) S_B [128,256) O_A [256,256+d) O_B [256+d,256+2d).
+// P_t (16-bit, two per column) overwrites the upper half of S_t.
+// Rescaling of O is lazy: the reference max only moves when the row max grows
+// by more than kRescaleLog2 (in log2 units). Using a stale, smaller reference
+// max is exact -- O and l share it and the final O / l cancels it -- and
+// bounds every P by 2^kRescaleLog2, so nothing overflows.
+#include "fa2_common.cuh"
+
+namespace fa2 {
+
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int SLAB_BYTES = kTileRows * 128;     // 128 rows x 128 bytes (64 elems)
+  static constexpr int TILE_BYTES = kTileRows * D * 2;   // one Q, K or V tile
+  static constexpr int NK = (D == 128) ? 2 : 4;          // K ring depth
+  static constexpr int NV = (D == 128) ? 2 : 4;          // V ring depth
+  static constexpr int OFF_Q = 0;                        // Q_A, Q_B
+  static constexpr int OFF_K = 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_V + NV * TILE_BYTES;
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;   // slack for 1024-byte alignment
+  static constexpr int THREADS = 384;
+  __host__ __device__ static constexpr uint32_t TM_S(int t) { return t ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t TM_O(int t) { return t ? 256u + D : 256u; }
+  static constexpr uint32_t TM_P_OFF = 64u;
+  static constexpr uint32_t TMEM_COLS = 512u;
+};
+
+template <int D>
+struct FwdShared {
+  uint64_t q_full;
+  uint64_t k_full[FwdCfg<D>::NK], k_empty[FwdCfg<D>::NK];
+  uint64_t v_full[FwdCfg<D>::NV], v_empty[FwdCfg<D>::NV];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// S_t = Q_t K^T : M=128 queries, N=128 keys, K=d. Both operands K-major,
+// 128-byte swizzled, one 64-element slab per 16 KiB.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  constexpr uint32_t idesc = make_idesc_f16(128, 128, BF16, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * FwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
+    umma_ss(d_tmem, make_sdesc_sw128(q_smem + off, 16, 1024),
+            make_sdesc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O_t (+)= P_t V : M=128 queries, N=d, K=128 keys. P from TMEM (16-bit pairs),
+// V is [key][d] in shared memory, i.e. MN-major for this product.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
+#pragma unroll
+  for (int kk = 0; kk < kTileRows / 16; ++kk) {
+    umma_ts(o_tmem, p_tmem + kk * 8,
+            make_sdesc_sw128(v_smem + kk * 2048, FwdCfg<D>::SLAB_BYTES, 1024), idesc,
+            (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void tma_load_tile(uint8_t* dst, const CUtensorMap* map,
+                                              uint64_t* bar, int row, int bh) {
+#pragma unroll
+  for (int s = 0; s < D / 64; ++s)
+    tma_load_3d(dst + s * FwdCfg<D>::SLAB_BYTES, map, bar, s * 64, row, bh);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                   const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ FwdShared<D> sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N;
+  const int mb = fwd_m_block_of(blockIdx.x, a.num_m_blocks, CAUSAL);
+  const int bh = blockIdx.y * a.H + blockIdx.z;  // grid = (m block, batch, head)
+  const int row0 = mb * kFwdRowsPerCta;
+  const int rows_a = min(kTileRows, N - row0);
+  const int rows_b = max(0, min(kTileRows, N - row0 - kTileRows));
+  const int n_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, N, CAUSAL),
+                      fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, N, CAUSAL)};
+  const int n_total = max(n_t[0], n_t[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.q_full, 1);
+    for (int i = 0; i < C::NK; ++i) { mbar_init(&sh.k_full[i], 1); mbar_init(&sh.k_empty[i], 1); }
+    for (int i = 0; i < C::NV; ++i) { mbar_init(&sh.v_full[i], 1); mbar_init(&sh.v_empty[i], 1); }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sh.s_full[t], 1);
+      mbar_init(&sh.p_full[t], 4);  // one arrival per softmax warp
+      mbar_init(&sh.o_full[t], 1);
+    }
+    mbar_init(&sh.mma_done, 1);
+    sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort_flag;
+  const WaitCtx wc{a.status, abort_flag, a.timeout_ns};
+
+  if (warp < 4) {
+    setmaxnreg_dec<64>();
+    if (warp == 0 && lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(&sh.q_full, (rows_b > 0 ? 2 : 1) * C::TILE_BYTES);
+      tma_load_tile<D>(smem + C::OFF_Q, &tm_q, &sh.q_full, row0, bh);
+      if (rows_b > 0)
+        tma_load_tile<D>(smem + C::OFF_Q + C::TILE_BYTES, &tm_q, &sh.q_full, row0 + kTileRows, bh);
+      int j = 0;
+      bool ok = true;
+      for (; j < n_total && ok; ++j) {
+        const int ks = j % C::NK, kp = (j / C::NK) & 1;
+        ok = mbar_wait(&sh.k_empty[ks], kp ^ 1, wc);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
+        tma_load_tile<D>(smem + C::OFF_K + ks * C::TILE_BYTES, &tm_k, &sh.k_full[ks], j * kTileRows, bh);
+        const int vs = j % C::NV, vp = (j / C::NV) & 1;
+        ok = mbar_wait(&sh.v_empty[vs], vp ^ 1, wc);
+        if (!ok) {
+          // K_j is in flight: let it land before leaving.
+          mbar_wait_drain(&sh.k_full[ks], kp, a.timeout_ns);
+          break;
+        }
+        if (a.fault == 1 && j == 0) continue;  // failure-path test: V_0 never arrives
+        mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
+        tma_load_tile<D>(smem + C::OFF_V + vs * C::TILE_BYTES, &tm_v, &sh.v_full[vs], j * kTileRows, bh);
+      }
+      if (!ok) {
+        // Drain every copy that may still be in flight (the last NK/NV issued).
+        mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
+        for (int jj = max(0, j - C::NK); jj < j; ++jj)
+          mbar_wait_drain(&sh.k_full[jj % C::NK], (jj / C::NK) & 1, a.timeout_ns);
+        for (int jj = max(0, j - C::NV); jj < j; ++jj)
+          if (!(a.fault == 1 && jj == 0))
+            mbar_wait_drain(&sh.v_full[jj % C::NV], (jj / C::NV) & 1, a.timeout_ns);
+      }
+      if (a.tile_count != nullptr) {
+        const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        a.tile_count[cta] = j;
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------- tcgen05.mma issuer ----------------
+      const uint32_t q_s[2] = {smem_u32(smem + C::OFF_Q), smem_u32(smem + C::OFF_Q + C::TILE_BYTES)};
+      bool ok = mbar_wait(&sh.q_full, 0, wc);
+      ok = ok && mbar_wait(&sh.k_full[0], 0, wc);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t k0 = smem_u32(smem + C::OFF_K);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (n_t[t] > 0) {
+            issue_qk<D, BF16>(tmem + C::TM_S(t), q_s[t], k0);
+            umma_commit(&sh.s_full[t]);
+          }
+        }
+        umma_commit(&sh.k_empty[0]);
+      }
+      for (int j = 0; j < n_total && ok; ++j) {
+        const bool more = (j + 1 < n_total);
+        if (more) {
+          const int ks = (j + 1) % C::NK;
+          ok = mbar_wait(&sh.k_full[ks], ((j + 1) / C::NK) & 1, wc);
+          if (!ok) break;
+        }
+        const int vs = j % C::NV;
+        ok = mbar_wait(&sh.v_full[vs], (j / C::NV) & 1, wc);
+        if (!ok) break;
+        const uint32_t v_smem = smem_u32(smem + C::OFF_V + vs * C::TILE_BYTES);
+        const uint32_t k_next = smem_u32(smem + C::OFF_K + ((j + 1) % C::NK) * C::TILE_BYTES);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < n_t[t]) {
+            ok = mbar_wait(&sh.p_full[t], j & 1, wc);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv<D, BF16>(tmem + C::TM_O(t), tmem + C::TM_S(t) + C::TM_P_OFF, v_smem, j > 0);
+            umma_commit(&sh.o_full[t]);
+            if (j + 1 < n_t[t]) {
+              issue_qk<D, BF16>(tmem + C::TM_S(t), q_s[t], k_next);
+              umma_commit(&sh.s_full[t]);
+            }
+          }
+        }
+        if (!ok) break;
+        umma_commit(&sh.v_empty[vs]);
+        if (more) umma_commit(&sh.k_empty[(j + 1) % C::NK]);
+      }
+      // Every MMA this thread issued must complete before TMEM is released.
+      umma_commit(&sh.mma_done);
+      mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
+    }
+  } else {
+    setmaxnreg_inc<208>();
+    // ---------------- softmax warpgroups ----------------
+    const int t = (warp - 4) >> 2;  // 0: tile A, 1: tile B
+    const int quad = warp & 3;      // TMEM lane quadrant this warp may access
+    const int r = quad * 32 + lane; // row inside the tile == TMEM lane
+    const int row_base = row0 + t * kTileRows;
+    const int my_row = row_base + r;
+    const int nt = n_t[t];
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::TM_S(t);
+    const uint32_t t_p = t_s + C::TM_P_OFF;
+    const uint32_t t_o = tmem + lane_off + C::TM_O(t);
+    const float sl2 = a.scale_log2;
+    float m_ref = -INFINITY;  // reference max (raw score units) used by exp
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = mbar_wait(&sh.s_full[t], j & 1, wc);
+      if (!ok) break;
+      __syncwarp();  // the warp-collective TMEM loads below need a converged warp
+      tc_fence_after();
+      uint32_t s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tmem_ld_32x32b_x32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
+      tmem_wait_ld();
+      reg_fence(s);
+      // Mask keys past the sequence end and, on the diagonal tile, keys after the query.
+      const int kv0 = j * kTileRows;
+      const bool need_mask = (kv0 + kTileRows > N) || (CAUSAL && kv0 + kTileRows - 1 > row_base);
+      if (need_mask) {
+        const int lim = CAUSAL ? min(N - kv0, my_row - kv0 + 1) : (N - kv0);
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = __uint_as_float(s[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      const float m_new = fmaxf(m_ref, mx);
+      const bool rescale = (m_new - m_ref) * sl2 > kRescaleLog2;  // also true when m_ref = -inf
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = ex2_approx((m_ref - m_new) * sl2);
+        m_ref = m_new;
+      }
+      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * sl2;
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, neg));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, neg));
+        rs0 += p0;
+        rs1 += p1;
+        s[c] = pack_x2<BF16>(p0, p1);
+      }
+      l = l * alpha + (rs0 + rs1);
+      tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_st_32x32b_x32(t_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_wait_st();
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O_t still holds the sum up to tile j-1: wait for that product, then rescale.
+        ok = mbar_wait(&sh.o_full[t], (j - 1) & 1, wc);
+        if (!ok) break;
+        __syncwarp();
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(t_o + c, o);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.p_full[t]);
+    }
+    // ---------------- epilogue: O / l -> 16-bit, L = m + ln l ----------------
+    if (ok && nt > 0) ok = mbar_wait(&sh.o_full[t], (nt - 1) & 1, wc);
+    // Q_t's shared buffer is free (its last S product has completed): stage O
+    // there in the same 128-byte-swizzled layout and store it with TMA, which
+    // also clips rows past the sequence end.
+    uint8_t* stage = smem + C::OFF_Q + t * C::TILE_BYTES;
+    if (ok && nt > 0) {
+      __syncwarp();
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(t_o + c, o);
+        tmem_wait_ld();
+        reg_fence(o);
+        const int slab = c / 64;
+        const int chunk0 = (c % 64) / 8;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint4 val;
+          val.x = pack_x2<BF16>(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+          val.y = pack_x2<BF16>(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+          val.z = pack_x2<BF16>(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+          val.w = pack_x2<BF16>(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+          const int phys = (chunk0 + k) ^ (r & 7);
+          *reinterpret_cast<uint4*>(stage + slab * C::SLAB_BYTES + r * 128 + phys * 16) = val;
+        }
+      }
+      fence_proxy_async_smem();
+      if (my_row < N) a.lse[static_cast<size_t>(bh) * N + my_row] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
+    }
+    // Every warp of the group reaches this barrier on every path, aborted or not.
+    named_bar_sync(1 + t, 128);
+    if ((threadIdx.x & 127) == 0 && nt > 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int s = 0; s < D / 64; ++s)
+        tma_store_3d(&tm_o, stage + s * C::SLAB_BYTES, s * 64, row_base, bh);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host-side launcher (called by the C ABI after validation).
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const CUtensorMap& to, const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  auto kern = fa2_fwd_kernel<D, BF16, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_m_blocks, a.B, a.H);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
+                       cudaStream_t stream) {
+#define FA2_FWD_CASE(DD, BB, CC) \
+  if (d == DD && bf16 == BB && causal == CC) return launch_fwd_t<DD, BB, CC>(tq, tk, tv, to, a, stream);
+  FA2_FWD_CASE(64, true, false)
+  FA2_FWD_CASE(64, true, true)
+  FA2_FWD_CASE(64, false, false)
+  FA2_FWD_CASE(64, false, true)
+  FA2_FWD_CASE(128, true, false)
+  FA2_FWD_CASE(128, true, true)
+  FA2_FWD_CASE(128, false, false)
+  FA2_FWD_CASE(128, false, true)
+#undef FA2_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa2

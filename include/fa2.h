@@ -1,0 +1,154 @@
+/*
+ * fa2.h -- C ABI of libfa2.so: FlashAttention-2 exact multi-head attention,
+ * forward and backward, on one sm_103a (GB300) GPU.
+ *
+ * The operation (sources: the FlashAttention-2 write-ups
+ *   "FlashAttention学习笔记(2)" (amentiraz.github.io), sections "V2 的运作流程"
+ *       and "V2中的thread blocks排布";
+ *   "大猿搬砖简记" (damodev.csdn.net), the V2 forward / backward walk-throughs;
+ *   "flash-attention123和ring-attention" (blog.csdn.net), 优化1 - 优化4):
+ *
+ *   for every batch b and head h, with S = scale * Q K^T (N x N):
+ *     causal: S[i][j] = -inf for j > i   (top-left alignment, key j visible to query i iff j <= i)
+ *     O   = softmax_rows(S) V
+ *     L_i = ln(sum_j exp(S[i][j]))       (the logsumexp; the only softmax statistic stored)
+ *   backward, given dO:
+ *     P = exp(S - L), dV = P^T dO, dP = dO V^T, D_i = sum_c dO[i][c] * O[i][c],
+ *     dS = P o (dP - D), dQ = scale * dS K, dK = scale * dS^T Q.
+ *
+ * Layout of every tensor argument: contiguous row-major [B][H][N][d] of 16-bit
+ * floats (dtype FA2_FP16 or FA2_BF16); lse is contiguous fp32 [B][H][N].
+ * Q, K and V share the sequence length N (self-attention).
+ *
+ * Ownership: the caller allocates and owns every buffer, including the
+ * backward workspace. The library keeps only a per-device status word (a
+ * static device variable) and never frees caller memory.
+ *
+ * Execution: every compute entry point only enqueues work on `stream` (a
+ * cudaStream_t, or NULL for the legacy default stream) and returns; nothing
+ * synchronises the host. Outputs are fully overwritten, never accumulated into,
+ * and must not overlap any input.
+ *
+ * Errors: every entry point returns an fa2_status (int). Arguments are checked
+ * before anything is launched; on an error nothing is launched and no output
+ * is touched. A kernel never traps: a bounded wait that runs out writes
+ * FA2_ERR_DEVICE_TIMEOUT into the device status word, which
+ * fa2_get_device_status() reports.
+ */
+#ifndef FA2_H_
+#define FA2_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa2_status {
+  FA2_OK = 0,
+  FA2_ERR_INVALID_ARG = 1,    /* null pointer, B/H/N < 1, bad dtype/causal, scale not finite or <= 0 */
+  FA2_ERR_UNSUPPORTED = 2,    /* d not in {64, 128}, or a size beyond the documented limits */
+  FA2_ERR_ALIGNMENT = 3,      /* a tensor pointer not 16-byte aligned (lse: 4-byte; workspace: 256-byte) */
+  FA2_ERR_ARCH = 4,           /* current device is not compute capability 10.3 (sm_103) */
+  FA2_ERR_CUDA = 5,           /* a CUDA runtime / driver call or kernel launch failed */
+  FA2_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up on a bounded wait (see fa2_get_device_status) */
+  FA2_ERR_WORKSPACE = 7,      /* backward workspace missing or smaller than fa2_bwd_workspace_size */
+  FA2_ERR_OVERLAP = 8         /* an output buffer overlaps an input buffer */
+} fa2_status;
+
+typedef enum fa2_dtype { FA2_FP16 = 0, FA2_BF16 = 1 } fa2_dtype;
+
+/* Forward pass (FlashAttention-2 forward: Q rows outer, K/V tiles inner, online
+ * softmax with running max m and sum l, one division by l at the end, only
+ * L = m + ln l stored; fully masked causal K/V tiles skipped).
+ *   q, k, v : device, [B][H][N][d] dtype, 16-byte aligned, read only.
+ *   o       : device, [B][H][N][d] dtype, 16-byte aligned, written.
+ *   lse     : device, [B][H][N] fp32, 4-byte aligned, written (natural log).
+ *   B, H, N : >= 1; B <= 65535, H <= 65535, B*H*N < 2^31.
+ *   d       : 64 or 128.
+ *   causal  : 0 or 1.
+ *   scale   : finite, > 0 (usually 1/sqrt(d)).
+ *   dtype   : FA2_FP16 or FA2_BF16 (q, k, v, o share it).
+ *   stream  : cudaStream_t or NULL. */
+int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+            int d, int causal, float scale, int dtype, void* stream);
+
+/* Bytes of device workspace fa2_bwd needs: the fp32 row sums D = rowsum(dO o O)
+ * and L * log2(e), each [B*H][N rounded up to 128]. Returns 0 for invalid sizes. */
+size_t fa2_bwd_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass (FlashAttention-2 backward: D = rowsum(dO o O) first; then K/V
+ * column blocks outer, Q tiles inner, S and P recomputed from L, dK/dV
+ * accumulated on chip; dQ, which accumulates along the key direction, in fp32
+ * on chip by a query-tile worker of its own -- no atomics, bit-reproducible).
+ *   q, k, v, o, dO : device [B][H][N][d] dtype, 16-byte aligned (o and lse from fa2_fwd).
+ *   lse            : device [B][H][N] fp32.
+ *   dq, dk, dv     : device [B][H][N][d] dtype, 16-byte aligned, written.
+ *   workspace      : device, >= fa2_bwd_workspace_size(B,H,N,d) bytes, 256-byte
+ *                    aligned, scratch owned by the caller; contents on entry
+ *                    are ignored and on exit undefined.
+ *   other arguments as in fa2_fwd. */
+int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+            const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
+            float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa2_bwd, plus: phase_events (4 cudaEvent_t created by the caller, or NULL)
+ * are recorded on `stream` before the preprocessing kernel, between it and
+ * the dK/dV kernel, between that and the dQ kernel, and after it, so the
+ * caller can time each of the three kernels. */
+int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                  void* const* phase_events, void* stream);
+
+/* Synchronises `stream`, then returns and clears the current device's status
+ * word: FA2_OK, or FA2_ERR_DEVICE_TIMEOUT if any kernel since the last call
+ * gave up on a bounded wait, or FA2_ERR_CUDA if the synchronisation failed. */
+int fa2_get_device_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa2_status_string(int status);
+
+/* ---- Host-only queries of the work mapping (no GPU needed) ----------------
+ * Forward grid = (num_m_block, B, H), the row block varying fastest
+ * ("FlashAttention学习笔记(2)", V2中的thread blocks排布). Each CTA owns
+ * rows_per_cta = 256 query rows (two 128-row tiles). */
+int fa2_fwd_grid(int B, int H, int N, int grid_out[3], int* rows_per_cta);
+
+/* Query rows [*row_begin, *row_end) and the number of K/V tiles of 128 keys
+ * that forward CTA `block_x` loads (causal: fully masked tiles are skipped,
+ * "flash-attention123和ring-attention", 优化3). */
+int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_end,
+                       int* kv_tiles);
+
+/* Backward dK/dV grid = (num_n_block, B, H): one CTA per 128-key column block
+ * ("FlashAttention学习笔记(2)", Foward和backward中的thread block划分). */
+int fa2_bwd_grid(int B, int H, int N, int d, int grid_out[3], int* keys_per_cta,
+                 int* q_rows_per_tile);
+
+/* Keys [*key_begin, *key_end) of backward CTA `block_x` and the query tiles
+ * [*q_tile_begin, *q_tile_end) (of q_rows_per_tile rows) it visits. */
+int fa2_bwd_block_work(int block_x, int N, int d, int causal, int* key_begin, int* key_end,
+                       int* q_tile_begin, int* q_tile_end);
+
+/* ---- Diagnostics ----------------------------------------------------------
+ * fa2_fwd, plus: tile_counts (device int array with one slot per forward CTA,
+ * grid order x fastest, or NULL) receives the number of K/V tiles each CTA
+ * actually loaded. */
+int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, int causal, float scale, int dtype, int* tile_counts,
+                         void* stream);
+
+/* Arms a host-side fault for the NEXT fa2_fwd / fa2_fwd_instrumented call on
+ * this process: kind 1 = the producer warp never loads the first V tile, so the
+ * MMA warp's wait on it runs out after timeout_ms (1..5000) milliseconds
+ * instead of the default 2 s; the kernel then records FA2_ERR_DEVICE_TIMEOUT
+ * and returns. kind 0 disarms. Exists to test the failure path without
+ * hanging or faulting the GPU. */
+int fa2_debug_arm_fault(int kind, int timeout_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_H_ */

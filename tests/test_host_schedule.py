@@ -1,0 +1,46 @@
+"""The library's host-side work mapping against the oracle's (CPU only):
+integer work, compared exactly."""
+
+import pytest
+
+from oracle import schedule
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 2, 512), (2, 3, 1), (1, 1, 1000), (4, 32, 8192),
+                                   (1, 2, 16384), (8, 16, 2048)])
+def test_fwd_grid_matches_oracle(fa2_lib, B, H, N):
+    (gx, gy, gz), rows = fa2_lib.fwd_grid(B, H, N)
+    assert (gx, gy, gz) == schedule.fwd_grid(B, H, N, rows)
+
+
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 255, 256, 257, 1000, 2048, 16384])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_block_work_matches_oracle(fa2_lib, N, causal):
+    (gx, _, _), rows = fa2_lib.fwd_grid(1, 1, N)
+    seen = []
+    prev = None
+    for bx in range(gx):
+        r0, r1, tiles = fa2_lib.fwd_block_work(bx, N, causal)
+        m = r0 // rows
+        assert r0 == m * rows and r1 == min(N, r0 + rows)
+        j0, j1 = schedule.fwd_kv_tile_range(m, N, rows, 128, causal)
+        assert j0 == 0 and tiles == j1
+        seen.append(m)
+        if causal and prev is not None:
+            assert tiles <= prev  # longest first
+        prev = tiles
+    assert sorted(seen) == list(range(gx))
+    if not causal:
+        assert seen == list(range(gx))  # the pages' order, row block fastest
+
+
+@pytest.mark.parametrize("N", [1, 63, 64, 65, 128, 129, 1000, 4096])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_block_work_matches_oracle(fa2_lib, N, d, causal):
+    (gx, gy, gz), keys, qrows = fa2_lib.bwd_grid(2, 3, N, d)
+    assert (gx, gy, gz) == schedule.bwd_grid(2, 3, N, keys)
+    for bx in range(gx):
+        k0, k1, i0, i1 = fa2_lib.bwd_block_work(bx, N, d, causal)
+        assert (k0, k1) == (bx * keys, min(N, (bx + 1) * keys))
+        assert (i0, i1) == schedule.bwd_q_tile_range(bx, N, qrows, keys, causal)
