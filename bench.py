@@ -1,0 +1,381 @@
+#!/usr/bin/env python3
+"""Throughput of one FlashAttention-2 training step (forward + backward) on GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+fa2_fwd (O, L) then fa2_bwd (D preprocessing, the K/V-outer dK/dV kernel, the
+Q-outer dQ kernel). The metric is TFLOP/s with the usual FLOP convention
+(forward 4*B*H*N^2*d, halved under the causal mask; backward 2.5x forward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fa2|reference]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs the same
+workload on its own GPU with its own seed (independent heads, no collective
+on the data path); the timed region is bracketed by a barrier and
+torch.cuda.synchronize() and the slowest rank's time is used.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "attention fwd/bwd TFLOPS on 1 GB300 (causal & not); % of dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_TRAFFIC = ROOT / "profiles" / "traffic.json"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=None)
+    p.add_argument("--impl", default="fa2", choices=["fa2", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--cpu-sample-heads", type=int, default=3)
+    return p.parse_args()
+
+
+def peaks():
+    f = ROOT / "MEASURED_PEAKS.json"
+    if f.exists():
+        d = json.loads(f.read_text())
+        return {"hbm_gbs": d["hbm_gbs"], "bf16": d["bf16_tflops"],
+                "bf16_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def source_sha() -> str:
+    """Hash of the CUDA sources: recorded ncu counters are only used while it matches."""
+    h = hashlib.sha256()
+    for p in sorted((ROOT / "exact_attention_64_gb300" / "csrc").glob("*")):
+        h.update(p.name.encode())
+        h.update(p.read_bytes())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(w, heads: int):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: the
+    first `heads` heads, forward + backward. Returns TFLOP/s in the metric's
+    FLOP convention."""
+    import torch
+
+    import oracle
+    from exact_attention_64_gb300.workloads import make_inputs
+
+    q, k, v, do = make_inputs(1, heads, w.N, w.d, w.torch_dtype, w.q_std, seed=0)
+    f = lambda t: t.to(torch.float64).numpy()  # noqa: E731
+    q, k, v, do = map(f, (q, k, v, do))
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, causal=w.causal, scale=w.scale)
+    oracle.backward(q, k, v, do, causal=w.causal, scale=w.scale)
+    dt = time.perf_counter() - t0
+    per_head = (w.fwd_flops() + w.bwd_flops()) / (w.B * w.H)
+    return {"value": per_head * heads / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} heads (N={w.N}, d={w.d}), fwd+bwd in fp64 NumPy, "
+                      f"{dt:.2f} s",
+            "seconds": dt}
+
+
+def run_reference(args, w, rank, world):
+    """The reference arm: the fp64 oracle on the host cores, one head per step."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_baseline(w, 1)
+    steps = [cpu_baseline(w, 1) for _ in range(args.steps)]
+    total = sum(s["seconds"] for s in steps)
+    per_head = (w.fwd_flops() + w.bwd_flops()) / (w.B * w.H)
+    value = per_head * len(steps) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "q_std": w.q_std, "step": "one (batch, head) of the workload, fwd+bwd"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": "one head of the workload per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from exact_attention_64_gb300.workloads import HEADLINE, WORKLOADS
+
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_64_gb300 as fa2
+    from exact_attention_64_gb300 import build as _build
+    from exact_attention_64_gb300.workloads import workload_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    _build.build()
+    lib = fa2.load_library()
+
+    B, H, N, d = w.B, w.H, w.N, w.d
+    dt_code = 1 if w.dtype == "bf16" else 0
+    q, k, v, do = (t.to(dev) for t in workload_inputs(w, seed=rank))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa2.bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    scale = w.scale
+    causal = int(w.causal)
+
+    def fwd():
+        c = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
+                        N, d, causal, scale, dt_code, sp)
+        if c:
+            raise fa2.FA2Error("fa2_fwd", c)
+
+    def bwd(ev_handles=None):
+        evp = None
+        if ev_handles is not None:
+            arr = (ctypes.c_void_p * 4)(*ev_handles)
+            evp = ctypes.cast(arr, ctypes.c_void_p)
+        c = lib.fa2_bwd_timed(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, d, causal, scale, dt_code, ws.data_ptr(),
+                              ws_bytes, evp, sp)
+        if c:
+            raise fa2.FA2Error("fa2_bwd", c)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    if fa2.device_status() != 0:
+        raise SystemExit("device status error during warm-up")
+
+    # ---- timed region: K steps, per-kernel events on the launching stream ----
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    fwd_ev = [(E(), E()) for _ in range(args.steps)]
+    bwd_ev = [[E(), E(), E(), E()] for _ in range(args.steps)]
+    t0, t1 = E(), E()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            fwd_ev[s][0].record(stream)
+            fwd()
+            fwd_ev[s][1].record(stream)
+            bwd([e.cuda_event for e in bwd_ev[s]])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    if fa2.device_status() != 0:
+        raise SystemExit("device status error in the timed region")
+    t_fwd = [a.elapsed_time(b) for a, b in fwd_ev]
+    t_pre = [e[0].elapsed_time(e[1]) for e in bwd_ev]
+    t_kv = [e[1].elapsed_time(e[2]) for e in bwd_ev]
+    t_dq = [e[2].elapsed_time(e[3]) for e in bwd_ev]
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    flops_step = w.fwd_flops() + w.bwd_flops()
+    value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+    pk = peaks()
+    mean = statistics.mean
+    # Algorithmic work per launch. The convention counts the forward as two
+    # N x N x d GEMM units (S, PV) and the backward as five (2.5x): the dK/dV
+    # kernel performs four of them (S^T, dP^T, dV, dK); the dQ kernel performs
+    # the fifth (dQ) plus two recomputations (S, dP) that the convention does
+    # not count, so only one unit is credited to it.
+    fw = w.fwd_flops()
+    kernels = {
+        "fa2_fwd_kernel": (mean(t_fwd), fw, "tensor"),
+        "fa2_bwd_dkdv_kernel": (mean(t_kv), 2.0 * fw, "tensor"),
+        "fa2_bwd_dq_kernel": (mean(t_dq), 0.5 * fw, "tensor"),
+        "fa2_bwd_pre_kernel": (mean(t_pre), B * H * N * (2 * d * 2 + 4 + 8), "hbm"),
+    }
+    dom = max(kernels, key=lambda n: kernels[n][0])
+    ms, work, bound = kernels[dom]
+    traffic = None
+    if PROFILE_TRAFFIC.exists():
+        tr = json.loads(PROFILE_TRAFFIC.read_text())
+        ent = tr.get("kernels", {}).get(dom)
+        if ent and tr.get("source_sha") == source_sha() and ent.get("workload") == w.name:
+            traffic = ent.get("bytes_per_launch")
+    if bound == "tensor":
+        achieved = work / (ms * 1e-3) / 1e12
+        peak = pk["bf16_sustained"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "peak_kind": f"bf16 sustained ({pk['source']})"}
+    else:
+        achieved = work / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "kernel": dom,
+                "peak_kind": f"hbm copy ({pk['source']})"}
+    tot = sum(x[0] for x in kernels.values())
+    per_kernel = {n: {"ms": t, "share": t / tot} for n, (t, _, _) in kernels.items()}
+    fwd_tf = fw / (mean(t_fwd) * 1e-3) / 1e12
+    bwd_tf = w.bwd_flops() / ((mean(t_pre) + mean(t_kv) + mean(t_dq)) * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+        ho, hdq, hdk, hdv = (torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(4))
+        hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+        d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+
+        def e2e_step():
+            for hsrc, ddst in ((hq, q), (hk, k), (hv, v), (hdo, do)):
+                ddst.copy_(hsrc, non_blocking=True)
+            fwd()
+            bwd()
+            for dsrc, hdst in ((o, ho), (lse, hlse), (dq, hdq), (dk, hdk), (dv, hdv)):
+                hdst.copy_(dsrc, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a, b = E(), E()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": flops_step * world * args.steps / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_sample_heads)
+        cpu.pop("seconds", None)
+
+    step_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do, o, dq, dk, dv))
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "q_std": w.q_std, "parallelism": f"head-sharded replicas x{world}",
+                   "l2": f"inputs larger than L2 ({step_bytes / 2**20:.0f} MiB touched per step "
+                         f"> {L2_BYTES / 2**20:.0f} MiB)"},
+        "detail": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+                   "fwd_frac_of_peak": fwd_tf / pk["bf16_sustained"],
+                   "bwd_frac_of_peak": bwd_tf / pk["bf16_sustained"],
+                   "peak_tflops": pk["bf16_sustained"], "per_kernel": per_kernel},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

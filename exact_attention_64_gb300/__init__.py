@@ -46,7 +46,10 @@ class FA2Error(RuntimeError):
 
     def __init__(self, func: str, code: int):
         self.code = code
-        super().__init__(f"{func} failed: {status_string(code)} ({code})")
+        extra = ""
+        if code == 5:  # FA2_ERR_CUDA: name the underlying CUDA error
+            extra = f", cuda error {load_library().fa2_last_cuda_error()}"
+        super().__init__(f"{func} failed: {status_string(code)} ({code}{extra})")
 
 
 def load_library() -> ctypes.CDLL:
@@ -75,6 +78,7 @@ def load_library() -> ctypes.CDLL:
         "fa2_bwd_grid": (i, [i, i, i, i, _c_int_p, _c_int_p, _c_int_p]),
         "fa2_bwd_block_work": (i, [i, i, i, i, _c_int_p, _c_int_p, _c_int_p, _c_int_p]),
         "fa2_debug_arm_fault": (i, [i, i]),
+        "fa2_last_cuda_error": (i, []),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)

@@ -39,6 +39,12 @@ int g_arch_ok[kMaxDevices];        // 0 unknown, 1 sm_103, -1 other
 int* g_status_ptr[kMaxDevices];    // device address of g_device_status, per device
 int g_fault_kind = 0;              // armed by fa2_debug_arm_fault, consumed by the next fwd
 unsigned long long g_fault_timeout_ns = 0;
+thread_local int g_last_cuda_error = 0;  // last cudaError_t behind an FA2_ERR_CUDA, per thread
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return FA2_ERR_CUDA;
+}
 
 int current_device(int* dev) {
   return cudaGetDevice(dev) == cudaSuccess && *dev >= 0 && *dev < kMaxDevices ? FA2_OK
@@ -52,15 +58,16 @@ int device_setup(int* dev_out, int** status_out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_arch_ok[dev] == 0) {
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return FA2_ERR_CUDA;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
     g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
   if (g_arch_ok[dev] != 1) return FA2_ERR_ARCH;
   if (g_status_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return FA2_ERR_CUDA;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e);
     g_status_ptr[dev] = static_cast<int*>(p);
   }
   if (g_encode == nullptr) {
@@ -111,7 +118,11 @@ int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dt
                3, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? FA2_OK : FA2_ERR_CUDA;
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = 1000 + static_cast<int>(r);  // driver codes offset by 1000
+    return FA2_ERR_CUDA;
+  }
+  return FA2_OK;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -157,9 +168,12 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
       g_fault_kind = 0;
     }
   }
+  // A non-sticky error left in this thread by another caller would otherwise be
+  // reported as ours by the post-launch check.
+  (void)cudaGetLastError();
   const cudaError_t e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
                                         static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+  return e == cudaSuccess ? FA2_OK : cuda_fail(e);
 }
 
 }  // namespace
@@ -242,11 +256,12 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
+  (void)cudaGetLastError();  // see fwd_impl
   const cudaError_t e = fa2::launch_bwd(
       d, dtype == FA2_BF16, causal != 0, o, dO, lse, maps, a, dsum, l2,
       static_cast<cudaStream_t>(stream),
       reinterpret_cast<cudaEvent_t*>(const_cast<void**>(phase_events)));
-  return e == cudaSuccess ? FA2_OK : FA2_ERR_CUDA;
+  return e == cudaSuccess ? FA2_OK : cuda_fail(e);
 }
 
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -261,9 +276,11 @@ int fa2_get_device_status(void* stream) {
   int* status = nullptr;
   const int st = device_setup(&dev, &status);
   if (st != FA2_OK) return st;
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA2_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   int h = 0;
-  if (cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA2_ERR_CUDA;
+  e = cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (h != 0) {
     const int zero = 0;
     if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
@@ -309,6 +326,8 @@ int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_
   if (kv_tiles) *kv_tiles = fa2::fwd_kv_tile_end(r0, r1, N, causal);
   return FA2_OK;
 }
+
+int fa2_last_cuda_error(void) { return g_last_cuda_error; }
 
 int fa2_debug_arm_fault(int kind, int timeout_ms) {
   if (kind != 0 && kind != 1) return FA2_ERR_INVALID_ARG;

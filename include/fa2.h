@@ -139,6 +139,11 @@ int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, f
                          int H, int N, int d, int causal, float scale, int dtype, int* tile_counts,
                          void* stream);
 
+/* The CUDA runtime error code (cudaError_t; a driver CUresult plus 1000 for a
+ * failed tensor-map encode) behind the last FA2_ERR_CUDA this thread received,
+ * or 0. */
+int fa2_last_cuda_error(void);
+
 /* Arms a host-side fault for the NEXT fa2_fwd / fa2_fwd_instrumented call on
  * this process: kind 1 = the producer warp never loads the first V tile, so the
  * MMA warp's wait on it runs out after timeout_ms (1..5000) milliseconds
