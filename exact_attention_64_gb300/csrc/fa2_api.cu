@@ -55,6 +55,13 @@ int current_device(int* dev) {
 int device_setup(int* dev_out, int** status_out) {
   int dev = 0;
   if (current_device(&dev) != FA2_OK) return FA2_ERR_CUDA;
+  // Binds the device's primary context to the calling thread. The driver-API
+  // tensor-map encoder needs a current context, and a thread that has so far
+  // only used the runtime lazily (an autograd worker, say) may not have one.
+  {
+    const cudaError_t e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_arch_ok[dev] == 0) {
     int major = 0, minor = 0;
