@@ -244,6 +244,10 @@ def main():
     fwd_ev = [(E(), E()) for _ in range(args.steps)]
     bwd_ev = [[E(), E(), E(), E()] for _ in range(args.steps)]
     t0, t1 = E(), E()
+    # torch creates an event's CUDA handle on its first record(): record every
+    # event once here so the handles passed to the library are valid.
+    for ev in [t0, t1] + [x for pair in fwd_ev for x in pair] + [x for l4 in bwd_ev for x in l4]:
+        ev.record(stream)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
