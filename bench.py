@@ -39,7 +39,7 @@ PROFILE_TRAFFIC = ROOT / "profiles" / "traffic.json"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=None)
     p.add_argument("--impl", default="fa2", choices=["fa2", "reference"])
@@ -59,12 +59,13 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
-def source_sha() -> str:
-    """Hash of the CUDA sources: recorded ncu counters are only used while it matches."""
+def source_sha(files) -> str:
+    """Hash of a kernel's CUDA sources: recorded ncu counters are only used
+    while it matches."""
     h = hashlib.sha256()
-    for p in sorted((ROOT / "exact_attention_64_gb300" / "csrc").glob("*")):
-        h.update(p.name.encode())
-        h.update(p.read_bytes())
+    for f in files:
+        h.update(f.encode())
+        h.update((ROOT / "exact_attention_64_gb300" / "csrc" / f).read_bytes())
     return h.hexdigest()[:16]
 
 
@@ -84,7 +85,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -296,7 +297,8 @@ def main():
     if PROFILE_TRAFFIC.exists():
         tr = json.loads(PROFILE_TRAFFIC.read_text())
         ent = tr.get("kernels", {}).get(dom)
-        if ent and tr.get("source_sha") == source_sha() and ent.get("workload") == w.name:
+        if (ent and ent.get("workload") == w.name
+                and ent.get("source_sha") == source_sha(ent.get("files", []))):
             traffic = ent.get("bytes_per_launch")
     if bound == "tensor":
         achieved = work / (ms * 1e-3) / 1e12

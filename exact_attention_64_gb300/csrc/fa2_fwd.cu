@@ -274,9 +274,16 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) s[c] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(s[0]);
+      // Row max as a tree of independent maxima (short dependency chains).
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
+      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[c + u]));
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = fmaxf(m_ref, mx);
       const bool rescale = (m_new - m_ref) * sl2 > kRescaleLog2;  // also true when m_ref = -inf
       float alpha = 1.f;
@@ -285,16 +292,16 @@ __global__ void __launch_bounds__(384, 1)
         m_ref = m_new;
       }
       const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * sl2;
-      float rs0 = 0.f, rs1 = 0.f;
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const float p0 = ex2_approx(fmaf(__uint_as_float(s[2 * c]), sl2, neg));
         const float p1 = ex2_approx(fmaf(__uint_as_float(s[2 * c + 1]), sl2, neg));
-        rs0 += p0;
-        rs1 += p1;
+        rs[(2 * c) & 7] += p0;
+        rs[(2 * c + 1) & 7] += p1;
         s[c] = pack_x2<BF16>(p0, p1);
       }
-      l = l * alpha + (rs0 + rs1);
+      l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
       tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
       tmem_st_32x32b_x32(t_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
       tmem_wait_st();
