@@ -101,6 +101,30 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
                   void* const* phase_events, void* stream);
 
+/* fa2_bwd without a caller-provided workspace, for callers that must not
+ * allocate device memory: code running inside a memory pool or a framework
+ * allocator it does not own, or a process that fixes its device footprint at
+ * start-up and may not call cudaMalloc afterwards. (The FlashAttention-2 pages
+ * have no counterpart to this entry point; it is a property of this library.)
+ * The backward's scratch -- the row sums D and L*log2(e), 8 bytes per query
+ * row with rows padded to 128 per head -- lives in a 16 MiB array built into
+ * the library, one per GPU that loads it, held until the process exits.
+ *   arguments  : as fa2_bwd, minus the workspace.
+ *   limit      : fa2_bwd_workspace_size(B,H,N,d) <= 16 MiB (for example up to
+ *                B*H = 256 heads of N = 8192); larger sizes return
+ *                FA2_ERR_UNSUPPORTED and touch nothing.
+ *   set-up     : the first call on a device looks up the array's device
+ *                address with that device current; make that first call
+ *                before any stream capture.
+ *   concurrency: every call on a device shares the one array, so calls that
+ *                may overlap on the GPU (different streams, or different host
+ *                threads) race on it; serialise them. Nothing needs clearing
+ *                between calls: each call writes every scratch entry it reads.
+ *   allocation : none (no cudaMalloc, cudaFree or allocating library call). */
+int fa2_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                    int causal, float scale, int dtype, void* stream);
+
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: FA2_OK, or FA2_ERR_DEVICE_TIMEOUT if any kernel since the last call
  * gave up on a bounded wait, or FA2_ERR_CUDA if the synchronisation failed. */
