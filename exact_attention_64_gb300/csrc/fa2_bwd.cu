@@ -19,8 +19,9 @@
 //                         variant: no atomics, and dQ is bit-reproducible.
 //
 // Products (tcgen05, 16-bit operands, fp32 accumulate in TMEM):
-//   dK/dV kernel, per query tile i:  S^T = K Q_i^T, dP^T = V dO_i^T   (SS, M=128 keys, N=128 queries)
-//                                    dV += P^T dO_i, dK += dS^T Q_i   (TS, A from TMEM, M=128 keys, N=d)
+//   dK/dV kernel, per 64-query half h of tile i:
+//                                    S^T = K Q_ih^T, dP^T = V dO_ih^T (SS, M=128 keys, N=64 queries)
+//                                    dV += P^T dO_ih, dK += dS^T Q_ih (TS, A from TMEM, M=128 keys, N=d)
 //   dQ kernel, per K/V tile j:       S = Q K_j^T, dP = dO V_j^T        (SS, M=128 queries, N=128 keys)
 //                                    dQ += dS K_j                      (TS, A from TMEM, M=128 queries, N=d)
 // with P = exp2(S * scale*log2e - L*log2e) and dS = P o (dP - D).
@@ -57,7 +58,8 @@ struct BwdCfg {
 struct BwdKvShared {
   uint64_t kv_full;
   uint64_t s_full[2], s_empty[2];  // streamed pair ring (Q_i, dO_i)
-  uint64_t st_full, sm_done, mma_done;
+  uint64_t st_full[2], sm_done[2];  // per 64-query half of a tile
+  uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -163,6 +165,46 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uin
             idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// The two products S^T = K Q_h^T and dP^T = V dO_h^T of one 64-query half h
+// of a 128-row tile: M=128 keys, N=64 queries, K=d, both operands K-major.
+// The half's rows start 8 KiB into each 128-row slab (1024-byte aligned, so
+// the swizzle phase is unchanged). The two independent chains are issued
+// k-step by k-step so that they overlap in the tensor pipe.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_half_scores(uint32_t d_st, uint32_t d_dpt, uint32_t k_smem,
+                                                uint32_t v_smem, uint32_t q_smem, uint32_t do_smem,
+                                                int h) {
+  constexpr uint32_t idesc = make_idesc_f16(128, 64, BF16, false, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t oa = (kk / 4) * BwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
+    const uint32_t ob = oa + h * 8192;
+    umma_ss(d_st, make_sdesc_sw128(k_smem + oa, 16, 1024), make_sdesc_sw128(q_smem + ob, 16, 1024),
+            idesc, kk > 0 ? 1u : 0u);
+    umma_ss(d_dpt, make_sdesc_sw128(v_smem + oa, 16, 1024),
+            make_sdesc_sw128(do_smem + ob, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// dV += P^T dO_h and dK += dS^T Q_h for one 64-query half: TS, M=128 keys,
+// N=d, K=64 queries; A (P^T, dS^T: 16-bit pairs) in TMEM, B = the half's rows
+// [query][d] in shared memory (MN-major). The two chains are interleaved.
+template <int D, bool BF16>
+__device__ __forceinline__ void mma_half_grads(uint32_t d_dv, uint32_t d_dk, uint32_t a_pt,
+                                               uint32_t a_dst, uint32_t do_smem, uint32_t q_smem,
+                                               int h, bool accumulate) {
+  constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint32_t off = h * 8192 + kk * 2048;
+    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+    umma_ts(d_dv, a_pt + kk * 8, make_sdesc_sw128(do_smem + off, BwdCfg<D>::SLAB_BYTES, 1024),
+            idesc, acc);
+    umma_ts(d_dk, a_dst + kk * 8, make_sdesc_sw128(q_smem + off, BwdCfg<D>::SLAB_BYTES, 1024),
+            idesc, acc);
+  }
+}
+
 // Stage a 128 x d fp32 TMEM accumulator (this thread's lane = row r) as 16-bit
 // rows, multiplied by mul, into a 128-byte-swizzled tile in shared memory.
 template <int D, bool BF16>
@@ -191,7 +233,9 @@ __device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r
 // 2. dK / dV kernel (K/V outer, Q inner)
 // ---------------------------------------------------------------------------
 // Warp roles: warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 compute P^T and dS^T
-// for query columns [0,64) and [64,128) of each tile (TMEM lane = key).
+// for query columns [0,64) and [64,128) of each tile (TMEM lane = key). Each
+// 64-query half has its own S^T / dP^T products and barriers, so one
+// warpgroup's exponentials overlap the tensor core's work on the other half.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -214,8 +258,10 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
     for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
-    mbar_init(&sh.st_full, 1);
-    mbar_init(&sh.sm_done, 8);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&sh.st_full[h], 1);
+      mbar_init(&sh.sm_done[h], 4);  // the four warps of warpgroup h
+    }
     mbar_init(&sh.mma_done, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -258,39 +304,46 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- tcgen05.mma issuer ----------------
+      // Order per tile i: for each half h, once warpgroup h has written
+      // P^T / dS^T: dV, dK of (i, h), then S^T, dP^T of (i+1, h) into the
+      // buffer just consumed. Warpgroup h computes while the tensor core works
+      // on the other half.
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
       bool ok = mbar_wait(&sh.kv_full, 0, wc) && mbar_wait(&sh.s_full[0], 0, wc);
       if (ok) {
         tc_fence_after();
-        mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, smem_u32(smem + C::OFF_STR0));
-        mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, smem_u32(smem + C::OFF_STR1));
-        umma_commit(&sh.st_full);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          mma_half_scores<D, BF16>(tmem + C::KV_ST + 64 * h, tmem + C::KV_DPT + 64 * h, k_s, v_s,
+                                   smem_u32(smem + C::OFF_STR0), smem_u32(smem + C::OFF_STR1), h);
+          umma_commit(&sh.st_full[h]);
+        }
       }
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::NS;
-        ok = mbar_wait(&sh.sm_done, i & 1, wc);
-        if (!ok) break;
-        tc_fence_after();
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-        // P^T / dS^T of query block kk (16 queries) live in the first 32 columns
-        // of the 64-column half that holds that block.
-        const uint32_t pt_base = tmem + C::KV_ST, dst_base = tmem + C::KV_DPT;
-        mma_tmem_x_tile<D, BF16>(
-            tmem + C::KV_DV, [pt_base](int kk) { return pt_base + 64u * (kk / 4) + 8u * (kk % 4); },
-            do_s, i > 0);
-        mma_tmem_x_tile<D, BF16>(
-            tmem + C::KV_DK, [dst_base](int kk) { return dst_base + 64u * (kk / 4) + 8u * (kk % 4); },
-            q_s, i > 0);
-        umma_commit(&sh.s_empty[st]);
-        if (i + 1 < n_steps) {
-          const int sn = (i + 1) % C::NS;
-          ok = mbar_wait(&sh.s_full[sn], ((i + 1) / C::NS) & 1, wc);
+        const int sn = (i + 1) % C::NS;
+        const uint32_t qn_s = smem_u32(smem + C::OFF_STR0 + sn * C::TILE_BYTES);
+        const uint32_t don_s = smem_u32(smem + C::OFF_STR1 + sn * C::TILE_BYTES);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait(&sh.sm_done[h], i & 1, wc);
           if (!ok) break;
           tc_fence_after();
-          mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, smem_u32(smem + C::OFF_STR0 + sn * C::TILE_BYTES));
-          mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, smem_u32(smem + C::OFF_STR1 + sn * C::TILE_BYTES));
-          umma_commit(&sh.st_full);
+          mma_half_grads<D, BF16>(tmem + C::KV_DV, tmem + C::KV_DK, tmem + C::KV_ST + 64 * h,
+                                  tmem + C::KV_DPT + 64 * h, do_s, q_s, h, i > 0 || h > 0);
+          if (h == 1) umma_commit(&sh.s_empty[st]);
+          if (i + 1 < n_steps) {
+            if (h == 0) {
+              ok = mbar_wait(&sh.s_full[sn], ((i + 1) / C::NS) & 1, wc);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            mma_half_scores<D, BF16>(tmem + C::KV_ST + 64 * h, tmem + C::KV_DPT + 64 * h, k_s, v_s,
+                                     qn_s, don_s, h);
+            umma_commit(&sh.st_full[h]);
+          }
         }
       }
       umma_commit(&sh.mma_done);
@@ -311,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < n_steps; ++i) {
       const int q0 = (i_begin + i) * kTileRows;
       const int qc0 = q0 + 64 * wg;  // first query column of this warpgroup
-      ok = mbar_wait(&sh.st_full, i & 1, wc);
+      ok = mbar_wait(&sh.st_full[wg], i & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
@@ -356,7 +409,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.sm_done);
+      if (lane == 0) mbar_arrive(&sh.sm_done[wg]);
     }
     // ---------------- epilogue: dV, scale*dK -> 16-bit, TMA store ----------------
     if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
