@@ -122,6 +122,23 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def slowest_rank_ms(ms: float, dist=None, device=None) -> float:
+    """The timed region's duration on the slowest rank (the max over ranks)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms)
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step: float, world: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: work of all ranks over the slowest rank's time
+    (weak scaling: every rank processes its own heads)."""
+    return flops_per_rank_step * world * steps / (ms * 1e-3) / 1e12
+
+
 def cpu_baseline(w, heads: int):
     """The fp64 oracle, as it stands, on a bounded sample of the workload: the
     first `heads` heads, forward + backward. Returns TFLOP/s in the metric's
@@ -270,13 +287,10 @@ def main():
     t_pre = [e[0].elapsed_time(e[1]) for e in bwd_ev]
     t_kv = [e[1].elapsed_time(e[2]) for e in bwd_ev]
     t_dq = [e[2].elapsed_time(e[3]) for e in bwd_ev]
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, dist if world > 1 else None, dev)
 
     flops_step = w.fwd_flops() + w.bwd_flops()
-    value = flops_step * world * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(flops_step, world, args.steps, elapsed_ms)
     pk = peaks()
     mean = statistics.mean
     # Algorithmic work per launch. The convention counts the forward as two
@@ -344,12 +358,8 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": flops_step * world * args.steps / (e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e_ms = slowest_rank_ms(a.elapsed_time(b), dist if world > 1 else None, dev)
+        e2e = {"value": job_tflops(flops_step, world, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps}
 

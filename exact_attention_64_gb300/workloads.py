@@ -53,6 +53,9 @@ _W = [
     Workload("causal_bf16_b1h2_n16384_d128", 1, 2, 16384, 128, "bf16", True),
     Workload("causal_bf16_b4h32_n8192_d128_qstd3", 4, 32, 8192, 128, "bf16", True, 3.0),
 ]
+# Same per-head shape as the headline with fewer heads: a profiling case whose
+# inputs still exceed L2 but whose captures stay small.
+_W.append(Workload("causal_bf16_b2h16_n8192_d128_qstd3", 2, 16, 8192, 128, "bf16", True, 3.0))
 WORKLOADS = {w.name: w for w in _W}
 
 # Long-sequence, d=128 causal workload the throughput target is stated on.
