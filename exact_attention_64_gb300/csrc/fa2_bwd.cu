@@ -59,7 +59,8 @@ struct BwdKvShared {
   uint64_t kv_full;
   uint64_t s_full[2], s_empty[2];  // streamed pair ring (Q_i, dO_i)
   uint64_t st_full[2], sm_done[2];  // per 64-query half of a tile
-  uint64_t mma_done;
+  uint64_t gr_done[2];              // dV/dK of half h issued and complete: buffer h free
+  uint64_t mma_done;                // one arrival from each of the two MMA issuers
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -236,6 +237,7 @@ __device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r
 // for query columns [0,64) and [64,128) of each tile (TMEM lane = key). Each
 // 64-query half has its own S^T / dP^T products and barriers, so one
 // warpgroup's exponentials overlap the tensor core's work on the other half.
+// Warp 1 issues the score products and warp 2 the gradient products.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -261,8 +263,9 @@ __global__ void __launch_bounds__(384, 1)
     for (int h = 0; h < 2; ++h) {
       mbar_init(&sh.st_full[h], 1);
       mbar_init(&sh.sm_done[h], 4);  // the four warps of warpgroup h
+      mbar_init(&sh.gr_done[h], 1);
     }
-    mbar_init(&sh.mma_done, 1);
+    mbar_init(&sh.mma_done, 2);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -303,29 +306,42 @@ __global__ void __launch_bounds__(384, 1)
           mbar_wait_drain(&sh.s_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
       }
     } else if (warp == 1 && lane == 0) {
-      // ---------------- tcgen05.mma issuer ----------------
-      // Order per tile i: for each half h, once warpgroup h has written
-      // P^T / dS^T: dV, dK of (i, h), then S^T, dP^T of (i+1, h) into the
-      // buffer just consumed. Warpgroup h computes while the tensor core works
-      // on the other half.
+      // ---------------- tcgen05.mma issuer 1: score products ----------------
+      // S^T, dP^T of (i, h) into buffer h, once the dV/dK products of (i-1, h)
+      // -- which read buffer h -- have completed. Two issuing threads keep the
+      // narrow (N=64) score products from being limited by one thread's issue
+      // rate, and the explicit gr_done wait orders the buffer reuse.
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
-      bool ok = mbar_wait(&sh.kv_full, 0, wc) && mbar_wait(&sh.s_full[0], 0, wc);
-      if (ok) {
-        tc_fence_after();
+      bool ok = mbar_wait(&sh.kv_full, 0, wc);
+      for (int i = 0; i < n_steps && ok; ++i) {
+        const int st = i % C::NS;
+        ok = mbar_wait(&sh.s_full[st], (i / C::NS) & 1, wc);
+        if (!ok) break;
+        const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
+        const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          if (i > 0) {
+            ok = mbar_wait(&sh.gr_done[h], (i - 1) & 1, wc);
+            if (!ok) break;
+          }
+          tc_fence_after();
           mma_half_scores<D, BF16>(tmem + C::KV_ST + 64 * h, tmem + C::KV_DPT + 64 * h, k_s, v_s,
-                                   smem_u32(smem + C::OFF_STR0), smem_u32(smem + C::OFF_STR1), h);
+                                   q_s, do_s, h);
           umma_commit(&sh.st_full[h]);
         }
       }
+      umma_commit(&sh.mma_done);
+      mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------- tcgen05.mma issuer 2: gradient products ----------------
+      // dV += P^T dO_ih and dK += dS^T Q_ih once warpgroup h has written P^T and
+      // dS^T; the tile's Q/dO stage is released after its second half.
+      bool ok = true;
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::NS;
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-        const int sn = (i + 1) % C::NS;
-        const uint32_t qn_s = smem_u32(smem + C::OFF_STR0 + sn * C::TILE_BYTES);
-        const uint32_t don_s = smem_u32(smem + C::OFF_STR1 + sn * C::TILE_BYTES);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           ok = mbar_wait(&sh.sm_done[h], i & 1, wc);
@@ -333,17 +349,8 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           mma_half_grads<D, BF16>(tmem + C::KV_DV, tmem + C::KV_DK, tmem + C::KV_ST + 64 * h,
                                   tmem + C::KV_DPT + 64 * h, do_s, q_s, h, i > 0 || h > 0);
+          umma_commit(&sh.gr_done[h]);
           if (h == 1) umma_commit(&sh.s_empty[st]);
-          if (i + 1 < n_steps) {
-            if (h == 0) {
-              ok = mbar_wait(&sh.s_full[sn], ((i + 1) / C::NS) & 1, wc);
-              if (!ok) break;
-              tc_fence_after();
-            }
-            mma_half_scores<D, BF16>(tmem + C::KV_ST + 64 * h, tmem + C::KV_DPT + 64 * h, k_s, v_s,
-                                     qn_s, don_s, h);
-            umma_commit(&sh.st_full[h]);
-          }
         }
       }
       umma_commit(&sh.mma_done);
