@@ -65,9 +65,24 @@ struct BwdKvShared {
   int abort_flag;
 };
 
+// dQ kernel shared-memory plan: Q, dO resident; K_j in a 3-deep ring (it is
+// read by S(j) and, last, by dQ(j)); V_j in a 2-deep ring (read only by
+// dP(j), so it is freed early). 224 KiB at d = 128.
+template <int D>
+struct DqCfg {
+  static constexpr int TILE_BYTES = BwdCfg<D>::TILE_BYTES;
+  static constexpr int NK = 3, NV = 2;
+  static constexpr int OFF_Q = 0, OFF_DO = TILE_BYTES;
+  static constexpr int OFF_K = 2 * TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_V + NV * TILE_BYTES;
+  static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 118784) ? SMEM_BYTES + 1024 : 118784;
+};
+
 struct BwdQShared {
   uint64_t q_full;
-  uint64_t s_full[2], s_empty[2];  // streamed pair ring (K_j, V_j)
+  uint64_t k_full[3], k_empty[3];  // K_j ring
+  uint64_t v_full[2], v_empty[2];  // V_j ring
   uint64_t st_full, s_free, ds_full, mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -457,6 +472,7 @@ __global__ void __launch_bounds__(384, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a, int num_m_blocks) {
   using C = BwdCfg<D>;
+  using Q = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ BwdQShared sh;
@@ -470,7 +486,8 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
-    for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
+    for (int s = 0; s < Q::NK; ++s) { mbar_init(&sh.k_full[s], 1); mbar_init(&sh.k_empty[s], 1); }
+    for (int s = 0; s < Q::NV; ++s) { mbar_init(&sh.v_full[s], 1); mbar_init(&sh.v_empty[s], 1); }
     mbar_init(&sh.st_full, 1);
     mbar_init(&sh.s_free, 8);
     mbar_init(&sh.ds_full, 8);
@@ -496,55 +513,68 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&sh.q_full, 2 * C::TILE_BYTES);
-      load_tile<D>(smem + C::OFF_FIX0, &tm_q, &sh.q_full, q0, bh);
-      load_tile<D>(smem + C::OFF_FIX1, &tm_do, &sh.q_full, q0, bh);
-      int j = 0;
+      load_tile<D>(smem + Q::OFF_Q, &tm_q, &sh.q_full, q0, bh);
+      load_tile<D>(smem + Q::OFF_DO, &tm_do, &sh.q_full, q0, bh);
+      int j = 0, kj = 0, vj = 0;  // K_j / V_j loads issued
       bool ok = true;
       for (; j < n_kv; ++j) {
-        const int st = j % C::NS, ph = (j / C::NS) & 1;
-        ok = mbar_wait(&sh.s_empty[st], ph ^ 1, wc);
+        const int ks = j % Q::NK, vs = j % Q::NV;
+        ok = mbar_wait(&sh.k_empty[ks], ((j / Q::NK) & 1) ^ 1, wc);
         if (!ok) break;
-        mbar_arrive_expect_tx(&sh.s_full[st], 2 * C::TILE_BYTES);
-        load_tile<D>(smem + C::OFF_STR0 + st * C::TILE_BYTES, &tm_k, &sh.s_full[st], j * kTileRows, bh);
-        load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_v, &sh.s_full[st], j * kTileRows, bh);
+        mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
+        load_tile<D>(smem + Q::OFF_K + ks * C::TILE_BYTES, &tm_k, &sh.k_full[ks], j * kTileRows, bh);
+        kj = j + 1;
+        ok = mbar_wait(&sh.v_empty[vs], ((j / Q::NV) & 1) ^ 1, wc);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
+        load_tile<D>(smem + Q::OFF_V + vs * C::TILE_BYTES, &tm_v, &sh.v_full[vs], j * kTileRows, bh);
+        vj = j + 1;
       }
       if (!ok) {
         mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
-        for (int jj = max(0, j - C::NS); jj < j; ++jj)
-          mbar_wait_drain(&sh.s_full[jj % C::NS], (jj / C::NS) & 1, a.timeout_ns);
+        for (int jj = max(0, kj - Q::NK); jj < kj; ++jj)
+          mbar_wait_drain(&sh.k_full[jj % Q::NK], (jj / Q::NK) & 1, a.timeout_ns);
+        for (int jj = max(0, vj - Q::NV); jj < vj; ++jj)
+          mbar_wait_drain(&sh.v_full[jj % Q::NV], (jj / Q::NV) & 1, a.timeout_ns);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- tcgen05.mma issuer ----------------
-      const uint32_t q_s = smem_u32(smem + C::OFF_FIX0), do_s = smem_u32(smem + C::OFF_FIX1);
-      bool ok = mbar_wait(&sh.q_full, 0, wc) && mbar_wait(&sh.s_full[0], 0, wc);
+      const uint32_t q_s = smem_u32(smem + Q::OFF_Q), do_s = smem_u32(smem + Q::OFF_DO);
+      auto k_at = [&](int j) { return smem_u32(smem + Q::OFF_K + (j % Q::NK) * C::TILE_BYTES); };
+      auto v_at = [&](int j) { return smem_u32(smem + Q::OFF_V + (j % Q::NV) * C::TILE_BYTES); };
+      bool ok = mbar_wait(&sh.q_full, 0, wc) && mbar_wait(&sh.k_full[0], 0, wc) &&
+                mbar_wait(&sh.v_full[0], 0, wc);
       if (ok) {
         tc_fence_after();
-        mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, smem_u32(smem + C::OFF_STR0));
-        mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, smem_u32(smem + C::OFF_STR1));
+        mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, k_at(0));
+        mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, v_at(0));
         umma_commit(&sh.st_full);
+        umma_commit(&sh.v_empty[0]);  // V_0 is read by dP(0) only
       }
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int st = j % C::NS, b = j & 1;
+        const int b = j & 1;
         // S(j), dP(j) have been read into registers: issue the next pair at once.
         ok = mbar_wait(&sh.s_free, j & 1, wc);
         if (!ok) break;
         tc_fence_after();
         if (j + 1 < n_kv) {
-          const int sn = (j + 1) % C::NS;
-          ok = mbar_wait(&sh.s_full[sn], ((j + 1) / C::NS) & 1, wc);
+          const int jn = j + 1;
+          ok = mbar_wait(&sh.k_full[jn % Q::NK], (jn / Q::NK) & 1, wc) &&
+               mbar_wait(&sh.v_full[jn % Q::NV], (jn / Q::NV) & 1, wc);
           if (!ok) break;
           tc_fence_after();
-          mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, smem_u32(smem + C::OFF_STR0 + sn * C::TILE_BYTES));
-          mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, smem_u32(smem + C::OFF_STR1 + sn * C::TILE_BYTES));
+          mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, k_at(jn));
+          mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, v_at(jn));
           umma_commit(&sh.st_full);
+          umma_commit(&sh.v_empty[jn % Q::NV]);
         }
         ok = mbar_wait(&sh.ds_full, j & 1, wc);
         if (!ok) break;
         tc_fence_after();
         const uint32_t ds_col = tmem + C::Q_DS(b);
         mma_tmem_x_tile<D, BF16>(tmem + C::Q_DQ, [ds_col](int kk) { return ds_col + 8u * kk; },
-                                 smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES), j > 0);
-        umma_commit(&sh.s_empty[st]);
+                                 k_at(j), j > 0);
+        umma_commit(&sh.k_empty[j % Q::NK]);  // K_j's last reader is dQ(j)
       }
       umma_commit(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
@@ -603,7 +633,7 @@ __global__ void __launch_bounds__(384, 1)
     // ---------------- epilogue: scale * dQ -> 16-bit, TMA store ----------------
     if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
     // Every MMA has completed: the Q buffer is free for staging.
-    uint8_t* stage = smem + C::OFF_FIX0;
+    uint8_t* stage = smem + Q::OFF_Q;
     if (ok && wg == 0) {
       __syncwarp();
       tc_fence_after();
@@ -669,11 +699,12 @@ static cudaError_t launch_bwd_t(const void* o, const void* dO, const float* lse,
   if (ev) cudaEventRecord(ev[2], stream);
   {
     auto kern = fa2_bwd_dq_kernel<D, BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg<D>::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     const int nm = dq_num_m_blocks(a.N);
     dim3 grid(nm, a.B, a.H);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[6],
+    kern<<<grid, C::THREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[6],
                                                       a, nm);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
