@@ -42,7 +42,10 @@ struct BwdCfg {
   static constexpr int OFF_FIX1 = TILE_BYTES;
   static constexpr int OFF_STR0 = 2 * TILE_BYTES;       // streamed pair, NS stages each
   static constexpr int OFF_STR1 = OFF_STR0 + NS * TILE_BYTES;
-  static constexpr int SMEM_BYTES = OFF_STR1 + NS * TILE_BYTES;
+  // dK/dV kernel: per-warp copies of L*log2e and D for its 64 query columns
+  // (8 warps x 128 floats), read as shared-memory broadcasts.
+  static constexpr int OFF_LD = OFF_STR1 + NS * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_LD + 8 * 128 * 4;
   // >= 116 KiB so that at most one CTA (one 512-column TMEM allocation) lives on an SM.
   static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 118784) ? SMEM_BYTES + 1024 : 118784;
   static constexpr int THREADS = 384;
@@ -382,18 +385,30 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t t_st = tmem + lane_off + C::KV_ST + 64 * wg;
     const uint32_t t_dpt = tmem + lane_off + C::KV_DPT + 64 * wg;
     const float sl2 = a.scale_log2;
+    // This warp's copy of L*log2e [0,64) and D [64,128) for its 64 query columns.
+    float* ld_s = reinterpret_cast<float*>(smem + C::OFF_LD) + (warp - 4) * 128;
     bool ok = true;
     for (int i = 0; i < n_steps; ++i) {
       const int q0 = (i_begin + i) * kTileRows;
       const int qc0 = q0 + 64 * wg;  // first query column of this warpgroup
+      {
+        // Coalesced loads (they do not depend on S) before waiting for the scores.
+        const size_t row = static_cast<size_t>(bh) * a.n_pad + qc0 + 2 * lane;
+        const float2 l2v = *reinterpret_cast<const float2*>(a.l2_pad + row);
+        const float2 dv2 = *reinterpret_cast<const float2*>(a.dsum_pad + row);
+        __syncwarp();  // every lane is done with the previous step's values
+        *reinterpret_cast<float2*>(ld_s + 2 * lane) = l2v;
+        *reinterpret_cast<float2*>(ld_s + 64 + 2 * lane) = dv2;
+        __syncwarp();
+      }
       ok = mbar_wait(&sh.st_full[wg], i & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
       const bool need_mask = (CAUSAL && qc0 < n0 + kTileRows - 1) || (qc0 + 64 > N) ||
                              (n0 + kTileRows > N);
-      const float4* pl = reinterpret_cast<const float4*>(a.l2_pad + static_cast<size_t>(bh) * a.n_pad + qc0);
-      const float4* pd = reinterpret_cast<const float4*>(a.dsum_pad + static_cast<size_t>(bh) * a.n_pad + qc0);
+      const float4* pl = reinterpret_cast<const float4*>(ld_s);
+      const float4* pd = reinterpret_cast<const float4*>(ld_s + 64);
       uint32_t pp[32], dsp[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -405,7 +420,7 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence(dp);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 l4 = __ldg(pl + 8 * h + u), d4 = __ldg(pd + 8 * h + u);
+          const float4 l4 = pl[8 * h + u], d4 = pd[8 * h + u];
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
           float p[4], ds[4];
