@@ -19,9 +19,8 @@
 //                         variant: no atomics, and dQ is bit-reproducible.
 //
 // Products (tcgen05, 16-bit operands, fp32 accumulate in TMEM):
-//   dK/dV kernel, per 64-query half h of tile i:
-//                                    S^T = K Q_ih^T, dP^T = V dO_ih^T (SS, M=128 keys, N=64 queries)
-//                                    dV += P^T dO_ih, dK += dS^T Q_ih (TS, A from TMEM, M=128 keys, N=d)
+//   dK/dV kernel, per query tile i:  S^T = K Q_i^T, dP^T = V dO_i^T   (SS, M=128 keys, N=128 queries)
+//                                    dV += P^T dO_i, dK += dS^T Q_i   (TS, A from TMEM, M=128 keys, N=d)
 //   dQ kernel, per K/V tile j:       S = Q K_j^T, dP = dO V_j^T        (SS, M=128 queries, N=128 keys)
 //                                    dQ += dS K_j                      (TS, A from TMEM, M=128 queries, N=d)
 // with P = exp2(S * scale*log2e - L*log2e) and dS = P o (dP - D).
@@ -51,7 +50,7 @@ struct BwdCfg {
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   // dK/dV kernel TMEM: dV, dK accumulators, S^T and dP^T (P^T / dS^T overwrite
-  // the first 32 columns of each warpgroup's 64-column half).
+  // the first 32 columns of each warpgroup's 64-column quarter of the region).
   static constexpr uint32_t KV_DV = 0, KV_DK = D, KV_ST = 2 * D, KV_DPT = 2 * D + 128;
   // dQ kernel TMEM: S, dP, the dQ accumulator and two dS buffers.
   static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256;
@@ -61,9 +60,10 @@ struct BwdCfg {
 struct BwdKvShared {
   uint64_t kv_full;
   uint64_t s_full[2], s_empty[2];  // streamed pair ring (Q_i, dO_i)
-  uint64_t st_full[2], sm_done[2];  // per 64-query half of a tile
-  uint64_t gr_done[2];              // dV/dK of half h issued and complete: buffer h free
-  uint64_t mma_done;                // one arrival from each of the two MMA issuers
+  uint64_t st_full, dpt_full;      // S^T(i) / dP^T(i) products complete
+  uint64_t p_done, ds_done;        // all 8 compute warps wrote P^T(i) / dS^T(i)
+  uint64_t dv_done, dk_done;       // dV(i) / dK(i) complete: S^T / dP^T regions free
+  uint64_t mma_done;               // one arrival from each of the two MMA issuers
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -184,43 +184,49 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uin
             idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// The two products S^T = K Q_h^T and dP^T = V dO_h^T of one 64-query half h
-// of a 128-row tile: M=128 keys, N=64 queries, K=d, both operands K-major.
-// The half's rows start 8 KiB into each 128-row slab (1024-byte aligned, so
-// the swizzle phase is unchanged). The two independent chains are issued
-// k-step by k-step so that they overlap in the tensor pipe.
-template <int D, bool BF16>
-__device__ __forceinline__ void mma_half_scores(uint32_t d_st, uint32_t d_dpt, uint32_t k_smem,
-                                                uint32_t v_smem, uint32_t q_smem, uint32_t do_smem,
-                                                int h) {
-  constexpr uint32_t idesc = make_idesc_f16(128, 64, BF16, false, false);
+// P^T for 32 query columns q_first.. of key row kg (dK/dV kernel):
+// p[c] = exp2(S^T[c] * scale*log2e - (L*log2e)[c]). With MASK, pairs outside the
+// sequence or with key > query (causal) get 0. MASK is a template parameter so
+// that tiles off the diagonal run a loop with no per-element branches, which
+// would otherwise keep the exponentials from overlapping.
+template <bool MASK, bool CAUSAL>
+__device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const float* l_cols, float sl2,
+                                            int kg, int q_first, int N, float* p) {
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t oa = (kk / 4) * BwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
-    const uint32_t ob = oa + h * 8192;
-    umma_ss(d_st, make_sdesc_sw128(k_smem + oa, 16, 1024), make_sdesc_sw128(q_smem + ob, 16, 1024),
-            idesc, kk > 0 ? 1u : 0u);
-    umma_ss(d_dpt, make_sdesc_sw128(v_smem + oa, 16, 1024),
-            make_sdesc_sw128(do_smem + ob, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  for (int u = 0; u < 8; ++u) {
+    const float4 l4 = reinterpret_cast<const float4*>(l_cols)[u];
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * u + e;
+      float pv = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -lv[e]));
+      if constexpr (MASK) {
+        const int qq = q_first + c;
+        const bool dead = kg >= N || qq >= N || (CAUSAL && kg > qq);
+        pv = dead ? 0.f : pv;
+      }
+      p[c] = pv;
+    }
   }
 }
 
-// dV += P^T dO_h and dK += dS^T Q_h for one 64-query half: TS, M=128 keys,
-// N=d, K=64 queries; A (P^T, dS^T: 16-bit pairs) in TMEM, B = the half's rows
-// [query][d] in shared memory (MN-major). The two chains are interleaved.
-template <int D, bool BF16>
-__device__ __forceinline__ void mma_half_grads(uint32_t d_dv, uint32_t d_dk, uint32_t a_pt,
-                                               uint32_t a_dst, uint32_t do_smem, uint32_t q_smem,
-                                               int h, bool accumulate) {
-  constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
+// dS for 64 key columns of query row my_row (dQ kernel), packed to 16-bit
+// pairs: dS = P o (dP - D) with P = exp2(S * scale*log2e - L*log2e). With MASK,
+// keys at or past lim and rows past the sequence get P = 0.
+template <bool MASK, bool BF16>
+__device__ __forceinline__ void dq_ds_cols(const uint32_t (&s)[64], const uint32_t (&dp)[64], float sl2,
+                                           float l2, float dsum, int kc0, int lim, bool row_ok,
+                                           uint32_t (&dsp)[32]) {
 #pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    const uint32_t off = h * 8192 + kk * 2048;
-    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-    umma_ts(d_dv, a_pt + kk * 8, make_sdesc_sw128(do_smem + off, BwdCfg<D>::SLAB_BYTES, 1024),
-            idesc, acc);
-    umma_ts(d_dk, a_dst + kk * 8, make_sdesc_sw128(q_smem + off, BwdCfg<D>::SLAB_BYTES, 1024),
-            idesc, acc);
+  for (int c = 0; c < 64; c += 2) {
+    float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -l2));
+    float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -l2));
+    if constexpr (MASK) {
+      p0 = (!row_ok || kc0 + c >= lim) ? 0.f : p0;
+      p1 = (!row_ok || kc0 + c + 1 >= lim) ? 0.f : p1;
+    }
+    dsp[c / 2] = pack_x2<BF16>(p0 * (__uint_as_float(dp[c]) - dsum),
+                               p1 * (__uint_as_float(dp[c + 1]) - dsum));
   }
 }
 
@@ -251,11 +257,13 @@ __device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r
 // ---------------------------------------------------------------------------
 // 2. dK / dV kernel (K/V outer, Q inner)
 // ---------------------------------------------------------------------------
-// Warp roles: warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 compute P^T and dS^T
-// for query columns [0,64) and [64,128) of each tile (TMEM lane = key). Each
-// 64-query half has its own S^T / dP^T products and barriers, so one
-// warpgroup's exponentials overlap the tensor core's work on the other half.
-// Warp 1 issues the score products and warp 2 the gradient products.
+// Warp roles: warp 0 TMA; warp 1 issues the score products S^T(i), dP^T(i);
+// warp 2 issues the gradient products dV(i), dK(i); warps 4-7 and 8-11 compute
+// P^T and dS^T for query columns [0,64) and [64,128) of each tile (TMEM lane =
+// key). The tile is split by product rather than by query: the exponentials
+// of P^T(i) overlap dP^T(i) on the tensor core, dS^T(i) overlaps dV(i), and
+// S^T(i+1) is issued as soon as dV(i) has read P^T(i), so the tensor core
+// runs S^T, dP^T, dV, dK back to back with full-width (N=128) score products.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -278,11 +286,12 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
     for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(&sh.st_full[h], 1);
-      mbar_init(&sh.sm_done[h], 4);  // the four warps of warpgroup h
-      mbar_init(&sh.gr_done[h], 1);
-    }
+    mbar_init(&sh.st_full, 1);
+    mbar_init(&sh.dpt_full, 1);
+    mbar_init(&sh.p_done, 8);   // the eight compute warps
+    mbar_init(&sh.ds_done, 8);
+    mbar_init(&sh.dv_done, 1);
+    mbar_init(&sh.dk_done, 1);
     mbar_init(&sh.mma_done, 2);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -325,51 +334,57 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------- tcgen05.mma issuer 1: score products ----------------
-      // S^T, dP^T of (i, h) into buffer h, once the dV/dK products of (i-1, h)
-      // -- which read buffer h -- have completed. Two issuing threads keep the
-      // narrow (N=64) score products from being limited by one thread's issue
-      // rate, and the explicit gr_done wait orders the buffer reuse.
+      // S^T(i) overwrites the region that holds P^T(i-1), so it waits until
+      // dV(i-1) has completed; dP^T(i) likewise waits for dK(i-1).
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
       bool ok = mbar_wait(&sh.kv_full, 0, wc);
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::NS;
         ok = mbar_wait(&sh.s_full[st], (i / C::NS) & 1, wc);
+        if (ok && i > 0) ok = mbar_wait(&sh.dv_done, (i - 1) & 1, wc);
         if (!ok) break;
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (i > 0) {
-            ok = mbar_wait(&sh.gr_done[h], (i - 1) & 1, wc);
-            if (!ok) break;
-          }
+        tc_fence_after();
+        mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_s);
+        umma_commit(&sh.st_full);
+        if (i > 0) {
+          ok = mbar_wait(&sh.dk_done, (i - 1) & 1, wc);
+          if (!ok) break;
           tc_fence_after();
-          mma_half_scores<D, BF16>(tmem + C::KV_ST + 64 * h, tmem + C::KV_DPT + 64 * h, k_s, v_s,
-                                   q_s, do_s, h);
-          umma_commit(&sh.st_full[h]);
         }
+        mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_s);
+        umma_commit(&sh.dpt_full);
       }
       umma_commit(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
     } else if (warp == 2 && lane == 0) {
       // ---------------- tcgen05.mma issuer 2: gradient products ----------------
-      // dV += P^T dO_ih and dK += dS^T Q_ih once warpgroup h has written P^T and
-      // dS^T; the tile's Q/dO stage is released after its second half.
+      // dV += P^T dO_i once all eight compute warps have written P^T(i), then
+      // dK += dS^T Q_i after dS^T(i). By then every product that reads the
+      // tile's Q/dO stage has been issued (S^T, dP^T before the compute warps
+      // could finish), so the commit after dK(i) releases the stage.
       bool ok = true;
+      const uint32_t t_pt = tmem + C::KV_ST, t_dst = tmem + C::KV_DPT;
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::NS;
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait(&sh.sm_done[h], i & 1, wc);
-          if (!ok) break;
-          tc_fence_after();
-          mma_half_grads<D, BF16>(tmem + C::KV_DV, tmem + C::KV_DK, tmem + C::KV_ST + 64 * h,
-                                  tmem + C::KV_DPT + 64 * h, do_s, q_s, h, i > 0 || h > 0);
-          umma_commit(&sh.gr_done[h]);
-          if (h == 1) umma_commit(&sh.s_empty[st]);
-        }
+        ok = mbar_wait(&sh.p_done, i & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tmem_x_tile<D, BF16>(tmem + C::KV_DV,
+                                 [&](int kk) { return t_pt + 64 * (kk / 4) + 8 * (kk % 4); }, do_s,
+                                 i > 0);
+        umma_commit(&sh.dv_done);
+        ok = mbar_wait(&sh.ds_done, i & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tmem_x_tile<D, BF16>(tmem + C::KV_DK,
+                                 [&](int kk) { return t_dst + 64 * (kk / 4) + 8 * (kk % 4); }, q_s,
+                                 i > 0);
+        umma_commit(&sh.dk_done);
+        umma_commit(&sh.s_empty[st]);
       }
       umma_commit(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
@@ -401,52 +416,64 @@ __global__ void __launch_bounds__(384, 1)
         *reinterpret_cast<float2*>(ld_s + 64 + 2 * lane) = dv2;
         __syncwarp();
       }
-      ok = mbar_wait(&sh.st_full[wg], i & 1, wc);
+      ok = mbar_wait(&sh.st_full, i & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
       const bool need_mask = (CAUSAL && qc0 < n0 + kTileRows - 1) || (qc0 + 64 > N) ||
                              (n0 + kTileRows > N);
-      const float4* pl = reinterpret_cast<const float4*>(ld_s);
       const float4* pd = reinterpret_cast<const float4*>(ld_s + 64);
-      uint32_t pp[32], dsp[32];
+      // P^T for this warpgroup's 64 queries, kept in fp32 for dS^T.
+      float p[64];
+      uint32_t pk[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t s[32], dp[32];
-        tmem_ld_32x32b_x32(t_st + 32 * h, s);
-        tmem_ld_32x32b_x32(t_dpt + 32 * h, dp);
+        uint32_t sv[32];
+        tmem_ld_32x32b_x32(t_st + 32 * h, sv);
         tmem_wait_ld();
-        reg_fence(s);
-        reg_fence(dp);
+        reg_fence(sv);
+        if (need_mask)
+          dkdv_p_cols<true, CAUSAL>(sv, ld_s + 32 * h, sl2, kg, qc0 + 32 * h, N, p + 32 * h);
+        else
+          dkdv_p_cols<false, CAUSAL>(sv, ld_s + 32 * h, sl2, kg, qc0 + 32 * h, N, p + 32 * h);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 l4 = pl[8 * h + u], d4 = pd[8 * h + u];
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * u + e;
-            p[e] = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -lv[e]));
-            if (need_mask) {
-              const int qq = qc0 + 32 * h + c;
-              if (kg >= N || qq >= N || (CAUSAL && kg > qq)) p[e] = 0.f;
-            }
-            ds[e] = p[e] * (__uint_as_float(dp[c]) - dv[e]);
-          }
-          pp[16 * h + 2 * u] = pack_x2<BF16>(p[0], p[1]);
-          pp[16 * h + 2 * u + 1] = pack_x2<BF16>(p[2], p[3]);
-          dsp[16 * h + 2 * u] = pack_x2<BF16>(ds[0], ds[1]);
-          dsp[16 * h + 2 * u + 1] = pack_x2<BF16>(ds[2], ds[3]);
-        }
+        for (int j = 0; j < 16; ++j)
+          pk[16 * h + j] = pack_x2<BF16>(p[32 * h + 2 * j], p[32 * h + 2 * j + 1]);
       }
-      // Both 32-column halves have been read: overwrite the first 32 columns.
-      tmem_st_32x32b_x32(t_st, pp);
-      tmem_st_32x32b_x32(t_dpt, dsp);
+      // Both 32-column halves of S^T have been read: P^T goes to the first 32.
+      tmem_st_32x32b_x32(t_st, pk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.sm_done[wg]);
+      if (lane == 0) mbar_arrive(&sh.p_done);
+
+      ok = mbar_wait(&sh.dpt_full, i & 1, wc);
+      if (!ok) break;
+      __syncwarp();
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t dp[32];
+        tmem_ld_32x32b_x32(t_dpt + 32 * h, dp);
+        tmem_wait_ld();
+        reg_fence(dp);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float4 d4 = pd[8 * h + u];
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            ds[e] = p[32 * h + 4 * u + e] * (__uint_as_float(dp[4 * u + e]) - dv[e]);
+          pk[16 * h + 2 * u] = pack_x2<BF16>(ds[0], ds[1]);
+          pk[16 * h + 2 * u + 1] = pack_x2<BF16>(ds[2], ds[3]);
+        }
+      }
+      tmem_st_32x32b_x32(t_dpt, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.ds_done);
     }
     // ---------------- epilogue: dV, scale*dK -> 16-bit, TMA store ----------------
     if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
@@ -628,17 +655,10 @@ __global__ void __launch_bounds__(384, 1)
       const int lim = CAUSAL ? min(N, my_row + 1) : N;  // keys < lim are visible
       const bool row_ok = my_row < N;
       uint32_t dsp[32];
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -l2));
-        float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -l2));
-        if (need_mask) {
-          if (!row_ok || kc0 + c >= lim) p0 = 0.f;
-          if (!row_ok || kc0 + c + 1 >= lim) p1 = 0.f;
-        }
-        dsp[c / 2] = pack_x2<BF16>(p0 * (__uint_as_float(dp[c]) - dsum),
-                                   p1 * (__uint_as_float(dp[c + 1]) - dsum));
-      }
+      if (need_mask)
+        dq_ds_cols<true, BF16>(s, dp, sl2, l2, dsum, kc0, lim, row_ok, dsp);
+      else
+        dq_ds_cols<false, BF16>(s, dp, sl2, l2, dsum, kc0, lim, row_ok, dsp);
       tmem_st_32x32b_x32(tmem + lane_off + C::Q_DS(b) + 32 * wg, dsp);
       tmem_wait_st();
       tc_fence_before();
