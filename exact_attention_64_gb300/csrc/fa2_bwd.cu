@@ -160,14 +160,16 @@ __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, 
 
 // D[tmem] = A B^T over the head dimension: M=128 rows of A, N=128 rows of B,
 // K=d. Both tiles K-major, 128-byte swizzled (the forward's Q K^T form).
+// Like every MMA helper here, issued by a converged warp (one lane elected).
 template <int D, bool BF16>
 __device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
   constexpr uint32_t idesc = make_idesc_f16(128, 128, BF16, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * BwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
-    umma_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024),
-            make_sdesc_sw128(b_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    const uint64_t ad = make_sdesc_sw128(a_smem + off, 16, 1024);
+    const uint64_t bd = make_sdesc_sw128(b_smem + off, 16, 1024);
+    umma_ss_warp(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -179,9 +181,11 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uin
                                                 bool accumulate) {
   constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
 #pragma unroll
-  for (int kk = 0; kk < kTileRows / 16; ++kk)
-    umma_ts(d_tmem, a_col(kk), make_sdesc_sw128(x_smem + kk * 2048, BwdCfg<D>::SLAB_BYTES, 1024),
-            idesc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kTileRows / 16; ++kk) {
+    const uint64_t bd = make_sdesc_sw128(x_smem + kk * 2048, BwdCfg<D>::SLAB_BYTES, 1024);
+    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+    umma_ts_warp(d_tmem, a_col(kk), bd, idesc, acc);
+  }
 }
 
 // P^T for 32 query columns q_first.. of key row kg (dK/dV kernel):
@@ -332,34 +336,34 @@ __global__ void __launch_bounds__(384, 1)
         for (int ii = max(0, i - C::NS); ii < i; ++ii)
           mbar_wait_drain(&sh.s_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- tcgen05.mma issuer 1: score products ----------------
+    } else if (warp == 1) {
+      // ---------------- tcgen05.mma issuer 1 (whole warp, one lane issues): score products ----------------
       // S^T(i) overwrites the region that holds P^T(i-1), so it waits until
       // dV(i-1) has completed; dP^T(i) likewise waits for dK(i-1).
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
-      bool ok = mbar_wait(&sh.kv_full, 0, wc);
+      bool ok = mbar_wait_warp(&sh.kv_full, 0, wc);
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::NS;
-        ok = mbar_wait(&sh.s_full[st], (i / C::NS) & 1, wc);
-        if (ok && i > 0) ok = mbar_wait(&sh.dv_done, (i - 1) & 1, wc);
+        ok = mbar_wait_warp(&sh.s_full[st], (i / C::NS) & 1, wc);
+        if (ok && i > 0) ok = mbar_wait_warp(&sh.dv_done, (i - 1) & 1, wc);
         if (!ok) break;
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
         tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_s);
-        umma_commit(&sh.st_full);
+        umma_commit_warp(&sh.st_full);
         if (i > 0) {
-          ok = mbar_wait(&sh.dk_done, (i - 1) & 1, wc);
+          ok = mbar_wait_warp(&sh.dk_done, (i - 1) & 1, wc);
           if (!ok) break;
           tc_fence_after();
         }
         mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_s);
-        umma_commit(&sh.dpt_full);
+        umma_commit_warp(&sh.dpt_full);
       }
-      umma_commit(&sh.mma_done);
+      umma_commit_warp(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
-    } else if (warp == 2 && lane == 0) {
-      // ---------------- tcgen05.mma issuer 2: gradient products ----------------
+    } else if (warp == 2) {
+      // ---------------- tcgen05.mma issuer 2 (whole warp, one lane issues): gradient products ----------------
       // dV += P^T dO_i once all eight compute warps have written P^T(i), then
       // dK += dS^T Q_i after dS^T(i). By then every product that reads the
       // tile's Q/dO stage has been issued (S^T, dP^T before the compute warps
@@ -370,23 +374,21 @@ __global__ void __launch_bounds__(384, 1)
         const int st = i % C::NS;
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-        ok = mbar_wait(&sh.p_done, i & 1, wc);
+        ok = mbar_wait_warp(&sh.p_done, i & 1, wc);
         if (!ok) break;
         tc_fence_after();
-        mma_tmem_x_tile<D, BF16>(tmem + C::KV_DV,
-                                 [&](int kk) { return t_pt + 64 * (kk / 4) + 8 * (kk % 4); }, do_s,
-                                 i > 0);
-        umma_commit(&sh.dv_done);
-        ok = mbar_wait(&sh.ds_done, i & 1, wc);
+        mma_tmem_x_tile<D, BF16>(
+            tmem + C::KV_DV, [&](int kk) { return t_pt + 64 * (kk / 4) + 8 * (kk % 4); }, do_s, i > 0);
+        umma_commit_warp(&sh.dv_done);
+        ok = mbar_wait_warp(&sh.ds_done, i & 1, wc);
         if (!ok) break;
         tc_fence_after();
-        mma_tmem_x_tile<D, BF16>(tmem + C::KV_DK,
-                                 [&](int kk) { return t_dst + 64 * (kk / 4) + 8 * (kk % 4); }, q_s,
-                                 i > 0);
-        umma_commit(&sh.dk_done);
-        umma_commit(&sh.s_empty[st]);
+        mma_tmem_x_tile<D, BF16>(
+            tmem + C::KV_DK, [&](int kk) { return t_dst + 64 * (kk / 4) + 8 * (kk % 4); }, q_s, i > 0);
+        umma_commit_warp(&sh.dk_done);
+        umma_commit_warp(&sh.s_empty[st]);
       }
-      umma_commit(&sh.mma_done);
+      umma_commit_warp(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
     }
   } else {
@@ -579,46 +581,46 @@ __global__ void __launch_bounds__(384, 1)
         for (int jj = max(0, vj - Q::NV); jj < vj; ++jj)
           mbar_wait_drain(&sh.v_full[jj % Q::NV], (jj / Q::NV) & 1, a.timeout_ns);
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- tcgen05.mma issuer ----------------
+    } else if (warp == 1) {
+      // ---------------- tcgen05.mma issuer (the whole warp; one lane issues) ----------------
       const uint32_t q_s = smem_u32(smem + Q::OFF_Q), do_s = smem_u32(smem + Q::OFF_DO);
       auto k_at = [&](int j) { return smem_u32(smem + Q::OFF_K + (j % Q::NK) * C::TILE_BYTES); };
       auto v_at = [&](int j) { return smem_u32(smem + Q::OFF_V + (j % Q::NV) * C::TILE_BYTES); };
-      bool ok = mbar_wait(&sh.q_full, 0, wc) && mbar_wait(&sh.k_full[0], 0, wc) &&
-                mbar_wait(&sh.v_full[0], 0, wc);
+      bool ok = mbar_wait_warp(&sh.q_full, 0, wc) && mbar_wait_warp(&sh.k_full[0], 0, wc) &&
+                mbar_wait_warp(&sh.v_full[0], 0, wc);
       if (ok) {
         tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, k_at(0));
         mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, v_at(0));
-        umma_commit(&sh.st_full);
-        umma_commit(&sh.v_empty[0]);  // V_0 is read by dP(0) only
+        umma_commit_warp(&sh.st_full);
+        umma_commit_warp(&sh.v_empty[0]);  // V_0 is read by dP(0) only
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int b = j & 1;
         // S(j), dP(j) have been read into registers: issue the next pair at once.
-        ok = mbar_wait(&sh.s_free, j & 1, wc);
+        ok = mbar_wait_warp(&sh.s_free, j & 1, wc);
         if (!ok) break;
         tc_fence_after();
         if (j + 1 < n_kv) {
           const int jn = j + 1;
-          ok = mbar_wait(&sh.k_full[jn % Q::NK], (jn / Q::NK) & 1, wc) &&
-               mbar_wait(&sh.v_full[jn % Q::NV], (jn / Q::NV) & 1, wc);
+          ok = mbar_wait_warp(&sh.k_full[jn % Q::NK], (jn / Q::NK) & 1, wc) &&
+               mbar_wait_warp(&sh.v_full[jn % Q::NV], (jn / Q::NV) & 1, wc);
           if (!ok) break;
           tc_fence_after();
           mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, k_at(jn));
           mma_rows_x_rows<D, BF16>(tmem + C::Q_DP, do_s, v_at(jn));
-          umma_commit(&sh.st_full);
-          umma_commit(&sh.v_empty[jn % Q::NV]);
+          umma_commit_warp(&sh.st_full);
+          umma_commit_warp(&sh.v_empty[jn % Q::NV]);
         }
-        ok = mbar_wait(&sh.ds_full, j & 1, wc);
+        ok = mbar_wait_warp(&sh.ds_full, j & 1, wc);
         if (!ok) break;
         tc_fence_after();
         const uint32_t ds_col = tmem + C::Q_DS(b);
         mma_tmem_x_tile<D, BF16>(tmem + C::Q_DQ, [ds_col](int kk) { return ds_col + 8u * kk; },
-                                 k_at(j), j > 0);
-        umma_commit(&sh.k_empty[j % Q::NK]);  // K_j's last reader is dQ(j)
+                                       k_at(j), j > 0);
+        umma_commit_warp(&sh.k_empty[j % Q::NK]);  // K_j's last reader is dQ(j)
       }
-      umma_commit(&sh.mma_done);
+      umma_commit_warp(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
     }
   } else {

@@ -64,15 +64,16 @@ struct FwdShared {
 };
 
 // S_t = Q_t K^T : M=128 queries, N=128 keys, K=d. Both operands K-major,
-// 128-byte swizzled, one 64-element slab per 16 KiB.
+// 128-byte swizzled, one 64-element slab per 16 KiB. Issued by a converged
+// warp (one lane elected), like every MMA helper in this file.
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t idesc = make_idesc_f16(128, 128, BF16, false, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * FwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
-    umma_ss(d_tmem, make_sdesc_sw128(q_smem + off, 16, 1024),
-            make_sdesc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+    umma_ss_warp(d_tmem, make_sdesc_sw128(q_smem + off, 16, 1024),
+                 make_sdesc_sw128(k_smem + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
   }
 }
 
@@ -84,9 +85,9 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
   constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
 #pragma unroll
   for (int kk = 0; kk < kTileRows / 16; ++kk) {
-    umma_ts(o_tmem, p_tmem + kk * 8,
-            make_sdesc_sw128(v_smem + kk * 2048, FwdCfg<D>::SLAB_BYTES, 1024), idesc,
-            (accumulate || kk > 0) ? 1u : 0u);
+    umma_ts_warp(o_tmem, p_tmem + kk * 8,
+                 make_sdesc_sw128(v_smem + kk * 2048, FwdCfg<D>::SLAB_BYTES, 1024), idesc,
+                 (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -186,11 +187,11 @@ __global__ void __launch_bounds__(384, 1)
         const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
         a.tile_count[cta] = j;
       }
-    } else if (warp == 1 && lane == 0) {
-      // ---------------- tcgen05.mma issuer ----------------
+    } else if (warp == 1) {
+      // ---------------- tcgen05.mma issuer (the whole warp; one lane issues) ----------------
       const uint32_t q_s[2] = {smem_u32(smem + C::OFF_Q), smem_u32(smem + C::OFF_Q + C::TILE_BYTES)};
-      bool ok = mbar_wait(&sh.q_full, 0, wc);
-      ok = ok && mbar_wait(&sh.k_full[0], 0, wc);
+      bool ok = mbar_wait_warp(&sh.q_full, 0, wc);
+      ok = ok && mbar_wait_warp(&sh.k_full[0], 0, wc);
       if (ok) {
         tc_fence_after();
         const uint32_t k0 = smem_u32(smem + C::OFF_K);
@@ -198,43 +199,43 @@ __global__ void __launch_bounds__(384, 1)
         for (int t = 0; t < 2; ++t) {
           if (n_t[t] > 0) {
             issue_qk<D, BF16>(tmem + C::TM_S(t), q_s[t], k0);
-            umma_commit(&sh.s_full[t]);
+            umma_commit_warp(&sh.s_full[t]);
           }
         }
-        umma_commit(&sh.k_empty[0]);
+        umma_commit_warp(&sh.k_empty[0]);
       }
       for (int j = 0; j < n_total && ok; ++j) {
         const bool more = (j + 1 < n_total);
         if (more) {
           const int ks = (j + 1) % C::NK;
-          ok = mbar_wait(&sh.k_full[ks], ((j + 1) / C::NK) & 1, wc);
+          ok = mbar_wait_warp(&sh.k_full[ks], ((j + 1) / C::NK) & 1, wc);
           if (!ok) break;
         }
         const int vs = j % C::NV;
-        ok = mbar_wait(&sh.v_full[vs], (j / C::NV) & 1, wc);
+        ok = mbar_wait_warp(&sh.v_full[vs], (j / C::NV) & 1, wc);
         if (!ok) break;
         const uint32_t v_smem = smem_u32(smem + C::OFF_V + vs * C::TILE_BYTES);
         const uint32_t k_next = smem_u32(smem + C::OFF_K + ((j + 1) % C::NK) * C::TILE_BYTES);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (j < n_t[t]) {
-            ok = mbar_wait(&sh.p_full[t], j & 1, wc);
+            ok = mbar_wait_warp(&sh.p_full[t], j & 1, wc);
             if (!ok) break;
             tc_fence_after();
             issue_pv<D, BF16>(tmem + C::TM_O(t), tmem + C::TM_S(t) + C::TM_P_OFF, v_smem, j > 0);
-            umma_commit(&sh.o_full[t]);
+            umma_commit_warp(&sh.o_full[t]);
             if (j + 1 < n_t[t]) {
               issue_qk<D, BF16>(tmem + C::TM_S(t), q_s[t], k_next);
-              umma_commit(&sh.s_full[t]);
+              umma_commit_warp(&sh.s_full[t]);
             }
           }
         }
         if (!ok) break;
-        umma_commit(&sh.v_empty[vs]);
-        if (more) umma_commit(&sh.k_empty[(j + 1) % C::NK]);
+        umma_commit_warp(&sh.v_empty[vs]);
+        if (more) umma_commit_warp(&sh.k_empty[(j + 1) % C::NK]);
       }
-      // Every MMA this thread issued must complete before TMEM is released.
-      umma_commit(&sh.mma_done);
+      // Every MMA this warp issued must complete before TMEM is released.
+      umma_commit_warp(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
     }
   } else {
