@@ -49,8 +49,10 @@ struct BwdCfg {
   static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 118784) ? SMEM_BYTES + 1024 : 118784;
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  // dK/dV kernel TMEM: dV, dK accumulators, S^T and dP^T (P^T / dS^T overwrite
-  // the first 32 columns of each warpgroup's 64-column quarter of the region).
+  // dK/dV kernel TMEM: dV, dK accumulators, S^T and dP^T. A warpgroup owns 64
+  // query columns of each region; once it has read dP^T for 32 of its queries
+  // (half h), it writes those 32 columns back as 16 columns of P^T and 16 of
+  // dS^T (16-bit pairs): [P^T h0 | dS^T h0 | P^T h1 | dS^T h1].
   static constexpr uint32_t KV_DV = 0, KV_DK = D, KV_ST = 2 * D, KV_DPT = 2 * D + 128;
   // dQ kernel TMEM: S, dP, the dQ accumulator and two dS buffers.
   static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256;
@@ -60,9 +62,10 @@ struct BwdCfg {
 struct BwdKvShared {
   uint64_t kv_full;
   uint64_t s_full[2], s_empty[2];  // streamed pair ring (Q_i, dO_i)
-  uint64_t st_full, dpt_full;      // S^T(i) / dP^T(i) products complete
-  uint64_t p_done, ds_done;        // all 8 compute warps wrote P^T(i) / dS^T(i)
-  uint64_t dv_done, dk_done;       // dV(i) / dK(i) complete: S^T / dP^T regions free
+  uint64_t st_full, st_free;       // S^T(i) complete / read into registers by all 8 compute warps
+  uint64_t dpt_full;               // dP^T(i) complete
+  uint64_t pds_done[2];            // P^T(i), dS^T(i) of query half h written by all 8 warps
+  uint64_t gr_done;                // dV(i), dK(i) complete: the dP^T region is free
   uint64_t mma_done;               // one arrival from each of the two MMA issuers
   uint32_t tmem_base;
   int abort_flag;
@@ -189,28 +192,25 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uin
 }
 
 // P^T for 32 query columns q_first.. of key row kg (dK/dV kernel):
-// p[c] = exp2(S^T[c] * scale*log2e - (L*log2e)[c]). With MASK, pairs outside the
+// p[c] = exp2(S^T[c] * scale*log2e + nl_cols[c]), nl_cols = -(L*log2e) in registers. With MASK, pairs outside the
 // sequence or with key > query (causal) get 0. MASK is a template parameter so
 // that tiles off the diagonal run a loop with no per-element branches, which
 // would otherwise keep the exponentials from overlapping.
 template <bool MASK, bool CAUSAL>
-__device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const float* l_cols, float sl2,
+__device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const float* nl_cols, float sl2,
                                             int kg, int q_first, int N, float* p) {
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const float4 l4 = reinterpret_cast<const float4*>(l_cols)[u];
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int c = 4 * u + e;
-      float pv = ex2_approx(fmaf(__uint_as_float(sv[c]), sl2, -lv[e]));
-      if constexpr (MASK) {
-        const int qq = q_first + c;
-        const bool dead = kg >= N || qq >= N || (CAUSAL && kg > qq);
-        pv = dead ? 0.f : pv;
-      }
-      p[c] = pv;
+  for (int c = 0; c < 32; c += 2) {
+    const float2 x = f2_fma(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                            make_float2(sl2, sl2), make_float2(nl_cols[c], nl_cols[c + 1]));
+    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
+    if constexpr (MASK) {
+      const int q0 = q_first + c;
+      p0 = (kg >= N || q0 >= N || (CAUSAL && kg > q0)) ? 0.f : p0;
+      p1 = (kg >= N || q0 + 1 >= N || (CAUSAL && kg > q0 + 1)) ? 0.f : p1;
     }
+    p[c] = p0;
+    p[c + 1] = p1;
   }
 }
 
@@ -264,10 +264,11 @@ __device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r
 // Warp roles: warp 0 TMA; warp 1 issues the score products S^T(i), dP^T(i);
 // warp 2 issues the gradient products dV(i), dK(i); warps 4-7 and 8-11 compute
 // P^T and dS^T for query columns [0,64) and [64,128) of each tile (TMEM lane =
-// key). The tile is split by product rather than by query: the exponentials
-// of P^T(i) overlap dP^T(i) on the tensor core, dS^T(i) overlaps dV(i), and
-// S^T(i+1) is issued as soon as dV(i) has read P^T(i), so the tensor core
-// runs S^T, dP^T, dV, dK back to back with full-width (N=128) score products.
+// key). The compute warps read all of S^T(i) into registers first, which frees
+// its TMEM region for S^T(i+1) at once; P^T(i) and dS^T(i) then go into the
+// dP^T region after dP^T(i) has been read. The exponentials of P^T(i) thus
+// overlap dV/dK(i-1) and dP^T(i) on the tensor core, and the only chain from
+// one tile to the next is dP^T -> dS^T -> dV, dK -> dP^T.
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -291,11 +292,11 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sh.kv_full, 1);
     for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
     mbar_init(&sh.st_full, 1);
+    mbar_init(&sh.st_free, 8);  // the eight compute warps
     mbar_init(&sh.dpt_full, 1);
-    mbar_init(&sh.p_done, 8);   // the eight compute warps
-    mbar_init(&sh.ds_done, 8);
-    mbar_init(&sh.dv_done, 1);
-    mbar_init(&sh.dk_done, 1);
+    mbar_init(&sh.pds_done[0], 8);
+    mbar_init(&sh.pds_done[1], 8);
+    mbar_init(&sh.gr_done, 1);
     mbar_init(&sh.mma_done, 2);
     sh.abort_flag = 0;
     fence_mbar_init();
@@ -338,54 +339,71 @@ __global__ void __launch_bounds__(384, 1)
       }
     } else if (warp == 1) {
       // ---------------- tcgen05.mma issuer 1 (whole warp, one lane issues): score products ----------------
-      // S^T(i) overwrites the region that holds P^T(i-1), so it waits until
-      // dV(i-1) has completed; dP^T(i) likewise waits for dK(i-1).
+      // dP^T(i) overwrites the region that holds P^T/dS^T(i-1), so it waits for
+      // dV/dK(i-1); it is issued before S^T(i+1), which only needs the compute
+      // warps to have read S^T(i) (st_free), so the tile-to-tile chain is not
+      // held up behind the next tile's scores.
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
-      bool ok = mbar_wait_warp(&sh.kv_full, 0, wc);
-      for (int i = 0; i < n_steps && ok; ++i) {
-        const int st = i % C::NS;
-        ok = mbar_wait_warp(&sh.s_full[st], (i / C::NS) & 1, wc);
-        if (ok && i > 0) ok = mbar_wait_warp(&sh.dv_done, (i - 1) & 1, wc);
-        if (!ok) break;
-        const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
-        const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
+      auto q_at = [&](int i) { return smem_u32(smem + C::OFF_STR0 + (i % C::NS) * C::TILE_BYTES); };
+      auto do_at = [&](int i) { return smem_u32(smem + C::OFF_STR1 + (i % C::NS) * C::TILE_BYTES); };
+      bool ok = mbar_wait_warp(&sh.kv_full, 0, wc) && mbar_wait_warp(&sh.s_full[0], 0, wc);
+      if (ok) {
         tc_fence_after();
-        mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_s);
+        mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(0));
         umma_commit_warp(&sh.st_full);
+      }
+      for (int i = 0; i < n_steps && ok; ++i) {
         if (i > 0) {
-          ok = mbar_wait_warp(&sh.dk_done, (i - 1) & 1, wc);
+          ok = mbar_wait_warp(&sh.gr_done, (i - 1) & 1, wc);
           if (!ok) break;
           tc_fence_after();
         }
-        mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_s);
+        mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_at(i));
         umma_commit_warp(&sh.dpt_full);
+        if (i + 1 < n_steps) {
+          ok = mbar_wait_warp(&sh.s_full[(i + 1) % C::NS], ((i + 1) / C::NS) & 1, wc) &&
+               mbar_wait_warp(&sh.st_free, i & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+          mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(i + 1));
+          umma_commit_warp(&sh.st_full);
+        }
       }
       umma_commit_warp(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
     } else if (warp == 2) {
       // ---------------- tcgen05.mma issuer 2 (whole warp, one lane issues): gradient products ----------------
-      // dV += P^T dO_i once all eight compute warps have written P^T(i), then
-      // dK += dS^T Q_i after dS^T(i). By then every product that reads the
-      // tile's Q/dO stage has been issued (S^T, dP^T before the compute warps
-      // could finish), so the commit after dK(i) releases the stage.
+      // dV += P^T dO_i and dK += dS^T Q_i, in two steps: the 16-query blocks of
+      // query half h of both warpgroups as soon as all eight compute warps have
+      // written that half. S^T(i) and dP^T(i) completed before that, so the
+      // commit after dK(i) also releases the tile's Q/dO stage.
+      constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
       bool ok = true;
-      const uint32_t t_pt = tmem + C::KV_ST, t_dst = tmem + C::KV_DPT;
+      const uint32_t t_g = tmem + C::KV_DPT;
       for (int i = 0; i < n_steps && ok; ++i) {
         const int st = i % C::NS;
         const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
         const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-        ok = mbar_wait_warp(&sh.p_done, i & 1, wc);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          ok = mbar_wait_warp(&sh.pds_done[h], i & 1, wc);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int w = 0; w < 2; ++w)
+#pragma unroll
+            for (int sub = 0; sub < 2; ++sub) {
+              const int kk = 4 * w + 2 * h + sub;  // 16-query block of the tile
+              const uint32_t acc = (i > 0 || h > 0 || w > 0 || sub > 0) ? 1u : 0u;
+              const uint32_t col = t_g + 64 * w + 32 * h + 8 * sub;
+              umma_ts_warp(tmem + C::KV_DV, col,
+                           make_sdesc_sw128(do_s + kk * 2048, C::SLAB_BYTES, 1024), idesc, acc);
+              umma_ts_warp(tmem + C::KV_DK, col + 16,
+                           make_sdesc_sw128(q_s + kk * 2048, C::SLAB_BYTES, 1024), idesc, acc);
+            }
+        }
         if (!ok) break;
-        tc_fence_after();
-        mma_tmem_x_tile<D, BF16>(
-            tmem + C::KV_DV, [&](int kk) { return t_pt + 64 * (kk / 4) + 8 * (kk % 4); }, do_s, i > 0);
-        umma_commit_warp(&sh.dv_done);
-        ok = mbar_wait_warp(&sh.ds_done, i & 1, wc);
-        if (!ok) break;
-        tc_fence_after();
-        mma_tmem_x_tile<D, BF16>(
-            tmem + C::KV_DK, [&](int kk) { return t_dst + 64 * (kk / 4) + 8 * (kk % 4); }, q_s, i > 0);
-        umma_commit_warp(&sh.dk_done);
+        umma_commit_warp(&sh.gr_done);
         umma_commit_warp(&sh.s_empty[st]);
       }
       umma_commit_warp(&sh.mma_done);
@@ -402,7 +420,7 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t t_st = tmem + lane_off + C::KV_ST + 64 * wg;
     const uint32_t t_dpt = tmem + lane_off + C::KV_DPT + 64 * wg;
     const float sl2 = a.scale_log2;
-    // This warp's copy of L*log2e [0,64) and D [64,128) for its 64 query columns.
+    // This warp's copy of -L*log2e [0,64) and D [64,128) for its 64 query columns.
     float* ld_s = reinterpret_cast<float*>(smem + C::OFF_LD) + (warp - 4) * 128;
     bool ok = true;
     for (int i = 0; i < n_steps; ++i) {
@@ -414,40 +432,53 @@ __global__ void __launch_bounds__(384, 1)
         const float2 l2v = *reinterpret_cast<const float2*>(a.l2_pad + row);
         const float2 dv2 = *reinterpret_cast<const float2*>(a.dsum_pad + row);
         __syncwarp();  // every lane is done with the previous step's values
-        *reinterpret_cast<float2*>(ld_s + 2 * lane) = l2v;
+        *reinterpret_cast<float2*>(ld_s + 2 * lane) = make_float2(-l2v.x, -l2v.y);
         *reinterpret_cast<float2*>(ld_s + 64 + 2 * lane) = dv2;
         __syncwarp();
+      }
+      // Shared-memory loads return slowly while the score products stream their
+      // operands from shared memory, so -L*log2e (and D below) are loaded into
+      // registers ahead of the waits rather than inside the exponent loops.
+      float lreg[64];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float4 l4 = reinterpret_cast<const float4*>(ld_s)[u];
+        lreg[4 * u] = l4.x; lreg[4 * u + 1] = l4.y; lreg[4 * u + 2] = l4.z; lreg[4 * u + 3] = l4.w;
       }
       ok = mbar_wait(&sh.st_full, i & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
+      // All 64 columns of S^T into registers, then release the region for S^T(i+1).
+      uint32_t sv[64];
+      tmem_ld_32x32b_x32(t_st, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld_32x32b_x32(t_st + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_wait_ld();
+      reg_fence(sv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.st_free);
       const bool need_mask = (CAUSAL && qc0 < n0 + kTileRows - 1) || (qc0 + 64 > N) ||
                              (n0 + kTileRows > N);
-      const float4* pd = reinterpret_cast<const float4*>(ld_s + 64);
-      // P^T for this warpgroup's 64 queries, kept in fp32 for dS^T.
-      float p[64];
+      // P^T as 16-bit pairs; dS^T below is formed from these rounded values.
       uint32_t pk[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t sv[32];
-        tmem_ld_32x32b_x32(t_st + 32 * h, sv);
-        tmem_wait_ld();
-        reg_fence(sv);
+        float p[32];
+        const uint32_t(&sh_h)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&sv[32 * h]);
         if (need_mask)
-          dkdv_p_cols<true, CAUSAL>(sv, ld_s + 32 * h, sl2, kg, qc0 + 32 * h, N, p + 32 * h);
+          dkdv_p_cols<true, CAUSAL>(sh_h, lreg + 32 * h, sl2, kg, qc0 + 32 * h, N, p);
         else
-          dkdv_p_cols<false, CAUSAL>(sv, ld_s + 32 * h, sl2, kg, qc0 + 32 * h, N, p + 32 * h);
+          dkdv_p_cols<false, CAUSAL>(sh_h, lreg + 32 * h, sl2, kg, qc0 + 32 * h, N, p);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          pk[16 * h + j] = pack_x2<BF16>(p[32 * h + 2 * j], p[32 * h + 2 * j + 1]);
+        for (int j = 0; j < 16; ++j) pk[16 * h + j] = pack_x2<BF16>(p[2 * j], p[2 * j + 1]);
       }
-      // Both 32-column halves of S^T have been read: P^T goes to the first 32.
-      tmem_st_32x32b_x32(t_st, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.p_done);
+      float dreg[64];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float4 d4 = reinterpret_cast<const float4*>(ld_s + 64)[u];
+        dreg[4 * u] = d4.x; dreg[4 * u + 1] = d4.y; dreg[4 * u + 2] = d4.z; dreg[4 * u + 3] = d4.w;
+      }
 
       ok = mbar_wait(&sh.dpt_full, i & 1, wc);
       if (!ok) break;
@@ -459,23 +490,24 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld_32x32b_x32(t_dpt + 32 * h, dp);
         tmem_wait_ld();
         reg_fence(dp);
+        // These 32 dP^T columns have been read: they now take P^T (16 pairs)
+        // and dS^T = P^T o (dP^T - D) (16 pairs) for queries 32h..32h+31.
+        uint32_t out[32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float4 d4 = pd[8 * h + u];
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            ds[e] = p[32 * h + 4 * u + e] * (__uint_as_float(dp[4 * u + e]) - dv[e]);
-          pk[16 * h + 2 * u] = pack_x2<BF16>(ds[0], ds[1]);
-          pk[16 * h + 2 * u + 1] = pack_x2<BF16>(ds[2], ds[3]);
+        for (int j = 0; j < 16; ++j) {
+          const int c = 32 * h + 2 * j;
+          out[j] = pk[16 * h + j];
+          const float2 ds = f2_mul(unpack_x2<BF16>(pk[16 * h + j]),
+                                   f2_sub(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
+                                          make_float2(dreg[c], dreg[c + 1])));
+          out[16 + j] = pack_x2<BF16>(ds.x, ds.y);
         }
+        tmem_st_32x32b_x32(t_dpt + 32 * h, out);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.pds_done[h]);
       }
-      tmem_st_32x32b_x32(t_dpt, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.ds_done);
     }
     // ---------------- epilogue: dV, scale*dK -> 16-bit, TMA store ----------------
     if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);

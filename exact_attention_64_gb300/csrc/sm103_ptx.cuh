@@ -310,5 +310,45 @@ __device__ __forceinline__ uint32_t pack_x2(float lo, float hi) {
   if constexpr (kBF16) return pack_bf16x2(lo, hi);
   else return pack_f16x2(lo, hi);
 }
+// Packed fp32 pairs (two IEEE fp32 operations per instruction, round to nearest).
+__device__ __forceinline__ uint64_t f2_bits(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 f2_from_bits(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;"
+      : "=l"(r) : "l"(f2_bits(a.x, a.y)), "l"(f2_bits(b.x, b.y)), "l"(f2_bits(c.x, c.y)));
+  return f2_from_bits(r);
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a.x, a.y)), "l"(f2_bits(b.x, b.y)));
+  return f2_from_bits(r);
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a.x, a.y)), "l"(f2_bits(b.x, b.y)));
+  return f2_from_bits(r);
+}
+
+// Inverse of pack_x2: the two 16-bit values of a pair as floats.
+template <bool kBF16>
+__device__ __forceinline__ float2 unpack_x2(uint32_t v) {
+  if constexpr (kBF16) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+  } else {
+    float lo, hi;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(v));
+    return make_float2(lo, hi);
+  }
+}
 
 }  // namespace fa2
