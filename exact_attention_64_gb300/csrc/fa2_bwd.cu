@@ -61,7 +61,8 @@ struct BwdCfg {
 
 struct BwdKvShared {
   uint64_t kv_full;
-  uint64_t s_full[2], s_empty[2];  // streamed pair ring (Q_i, dO_i)
+  uint64_t q_full[2], do_full[2];  // streamed pair ring: Q_i and dO_i landed (separately, so
+  uint64_t s_empty[2];             // S^T(i) need not wait for dO_i); both free again
   uint64_t st_full, st_free;       // S^T(i) complete / read into registers by all 8 compute warps
   uint64_t dpt_full;               // dP^T(i) complete
   uint64_t pds_done[2];            // P^T(i), dS^T(i) of query half h written by all 8 warps
@@ -290,7 +291,11 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
-    for (int s = 0; s < C::NS; ++s) { mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 1); }
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&sh.q_full[s], 1);
+      mbar_init(&sh.do_full[s], 1);
+      mbar_init(&sh.s_empty[s], 1);
+    }
     mbar_init(&sh.st_full, 1);
     mbar_init(&sh.st_free, 8);  // the eight compute warps
     mbar_init(&sh.dpt_full, 1);
@@ -328,14 +333,17 @@ __global__ void __launch_bounds__(384, 1)
         ok = mbar_wait(&sh.s_empty[st], ph ^ 1, wc);
         if (!ok) break;
         const int q0 = (i_begin + i) * kTileRows;
-        mbar_arrive_expect_tx(&sh.s_full[st], 2 * C::TILE_BYTES);
-        load_tile<D>(smem + C::OFF_STR0 + st * C::TILE_BYTES, &tm_q, &sh.s_full[st], q0, bh);
-        load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_do, &sh.s_full[st], q0, bh);
+        mbar_arrive_expect_tx(&sh.q_full[st], C::TILE_BYTES);
+        load_tile<D>(smem + C::OFF_STR0 + st * C::TILE_BYTES, &tm_q, &sh.q_full[st], q0, bh);
+        mbar_arrive_expect_tx(&sh.do_full[st], C::TILE_BYTES);
+        load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_do, &sh.do_full[st], q0, bh);
       }
       if (!ok) {
         mbar_wait_drain(&sh.kv_full, 0, a.timeout_ns);
-        for (int ii = max(0, i - C::NS); ii < i; ++ii)
-          mbar_wait_drain(&sh.s_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
+        for (int ii = max(0, i - C::NS); ii < i; ++ii) {
+          mbar_wait_drain(&sh.q_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
+          mbar_wait_drain(&sh.do_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
+        }
       }
     } else if (warp == 1) {
       // ---------------- tcgen05.mma issuer 1 (whole warp, one lane issues): score products ----------------
@@ -346,22 +354,21 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
       auto q_at = [&](int i) { return smem_u32(smem + C::OFF_STR0 + (i % C::NS) * C::TILE_BYTES); };
       auto do_at = [&](int i) { return smem_u32(smem + C::OFF_STR1 + (i % C::NS) * C::TILE_BYTES); };
-      bool ok = mbar_wait_warp(&sh.kv_full, 0, wc) && mbar_wait_warp(&sh.s_full[0], 0, wc);
+      bool ok = mbar_wait_warp(&sh.kv_full, 0, wc) && mbar_wait_warp(&sh.q_full[0], 0, wc);
       if (ok) {
         tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(0));
         umma_commit_warp(&sh.st_full);
       }
       for (int i = 0; i < n_steps && ok; ++i) {
-        if (i > 0) {
-          ok = mbar_wait_warp(&sh.gr_done, (i - 1) & 1, wc);
-          if (!ok) break;
-          tc_fence_after();
-        }
+        ok = mbar_wait_warp(&sh.do_full[i % C::NS], (i / C::NS) & 1, wc) &&
+             (i == 0 || mbar_wait_warp(&sh.gr_done, (i - 1) & 1, wc));
+        if (!ok) break;
+        tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_at(i));
         umma_commit_warp(&sh.dpt_full);
         if (i + 1 < n_steps) {
-          ok = mbar_wait_warp(&sh.s_full[(i + 1) % C::NS], ((i + 1) / C::NS) & 1, wc) &&
+          ok = mbar_wait_warp(&sh.q_full[(i + 1) % C::NS], ((i + 1) / C::NS) & 1, wc) &&
                mbar_wait_warp(&sh.st_free, i & 1, wc);
           if (!ok) break;
           tc_fence_after();
