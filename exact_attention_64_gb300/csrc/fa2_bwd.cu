@@ -217,21 +217,25 @@ __device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const floa
 
 // dS for 64 key columns of query row my_row (dQ kernel), packed to 16-bit
 // pairs: dS = P o (dP - D) with P = exp2(S * scale*log2e - L*log2e). With MASK,
-// keys at or past lim and rows past the sequence get P = 0.
+// keys at or past lim and rows past the sequence get P = 0. Column pairs use
+// packed fp32 (f32x2) arithmetic.
 template <bool MASK, bool BF16>
 __device__ __forceinline__ void dq_ds_cols(const uint32_t (&s)[64], const uint32_t (&dp)[64], float sl2,
                                            float l2, float dsum, int kc0, int lim, bool row_ok,
                                            uint32_t (&dsp)[32]) {
+  const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(-l2, -l2);
+  const float2 dsum2 = make_float2(dsum, dsum);
 #pragma unroll
   for (int c = 0; c < 64; c += 2) {
-    float p0 = ex2_approx(fmaf(__uint_as_float(s[c]), sl2, -l2));
-    float p1 = ex2_approx(fmaf(__uint_as_float(s[c + 1]), sl2, -l2));
+    const float2 x = f2_fma(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nl2);
+    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
     if constexpr (MASK) {
       p0 = (!row_ok || kc0 + c >= lim) ? 0.f : p0;
       p1 = (!row_ok || kc0 + c + 1 >= lim) ? 0.f : p1;
     }
-    dsp[c / 2] = pack_x2<BF16>(p0 * (__uint_as_float(dp[c]) - dsum),
-                               p1 * (__uint_as_float(dp[c + 1]) - dsum));
+    const float2 ds = f2_mul(make_float2(p0, p1),
+                             f2_sub(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), dsum2));
+    dsp[c / 2] = pack_x2<BF16>(ds.x, ds.y);
   }
 }
 

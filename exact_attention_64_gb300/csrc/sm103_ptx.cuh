@@ -327,6 +327,11 @@ __device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
       : "=l"(r) : "l"(f2_bits(a.x, a.y)), "l"(f2_bits(b.x, b.y)), "l"(f2_bits(c.x, c.y)));
   return f2_from_bits(r);
 }
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a.x, a.y)), "l"(f2_bits(b.x, b.y)));
+  return f2_from_bits(r);
+}
 __device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
   uint64_t r;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a.x, a.y)), "l"(f2_bits(b.x, b.y)));
