@@ -365,15 +365,16 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit_warp(&sh.st_full);
       }
       for (int i = 0; i < n_steps && ok; ++i) {
-        ok = mbar_wait_warp(&sh.do_full[i % C::NS], (i / C::NS) & 1, wc) &&
-             (i == 0 || mbar_wait_warp(&sh.gr_done, (i - 1) & 1, wc));
+        ok = (i == 0) ? mbar_wait_warp(&sh.do_full[0], 0, wc)
+                      : mbar_wait2_warp(&sh.do_full[i % C::NS], (i / C::NS) & 1, &sh.gr_done,
+                                        (i - 1) & 1, wc);
         if (!ok) break;
         tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_at(i));
         umma_commit_warp(&sh.dpt_full);
         if (i + 1 < n_steps) {
-          ok = mbar_wait_warp(&sh.q_full[(i + 1) % C::NS], ((i + 1) / C::NS) & 1, wc) &&
-               mbar_wait_warp(&sh.st_free, i & 1, wc);
+          ok = mbar_wait2_warp(&sh.q_full[(i + 1) % C::NS], ((i + 1) / C::NS) & 1, &sh.st_free,
+                               i & 1, wc);
           if (!ok) break;
           tc_fence_after();
           mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(i + 1));
@@ -646,8 +647,8 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         if (j + 1 < n_kv) {
           const int jn = j + 1;
-          ok = mbar_wait_warp(&sh.k_full[jn % Q::NK], (jn / Q::NK) & 1, wc) &&
-               mbar_wait_warp(&sh.v_full[jn % Q::NV], (jn / Q::NV) & 1, wc);
+          ok = mbar_wait2_warp(&sh.k_full[jn % Q::NK], (jn / Q::NK) & 1, &sh.v_full[jn % Q::NV],
+                               (jn / Q::NV) & 1, wc);
           if (!ok) break;
           tc_fence_after();
           mma_rows_x_rows<D, BF16>(tmem + C::Q_S, q_s, k_at(jn));

@@ -12,10 +12,12 @@
 // that the causal mask hides completely are skipped, not loaded (优化3).
 //
 // GB300 mapping (one CTA = two 128-row Q tiles "A" and "B" of one head):
-//   warp 0        TMA producer: Q_A, Q_B once, then K_j, V_j through
-//                 multi-stage shared-memory rings (mbarrier full/empty pairs).
-//   warp 1        tcgen05.mma issuer (one thread): S_t = Q_t K_j^T into TMEM,
-//                 O_t += P_t V_j with P_t read straight from TMEM.
+//   warp 0        TMA producer: Q_A, Q_B once, then K_j through a multi-stage
+//                 shared-memory ring (mbarrier full/empty pairs).
+//   warp 3        TMA producer of the V_j ring.
+//   warp 1        tcgen05.mma issuer (the whole warp, one lane elected):
+//                 S_t = Q_t K_j^T into TMEM, O_t += P_t V_j with P_t read
+//                 straight from TMEM.
 //   warps 4-7     softmax of tile A, warps 8-11 softmax of tile B. TMEM lane i
 //                 is query row i, so one thread owns one whole row: the row max
 //                 and row sum need no shuffles. The two tiles ping-pong, so the
@@ -147,10 +149,11 @@ __global__ void __launch_bounds__(384, 1)
   if (warp < 4) {
     setmaxnreg_dec<64>();
     if (warp == 0 && lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer: Q, then the K ring ----------------
+      // K and V have producers of their own so that a V slot that frees late
+      // (V_j is read by the last products of step j) never holds up K_{j+1}.
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
       mbar_arrive_expect_tx(&sh.q_full, (rows_b > 0 ? 2 : 1) * C::TILE_BYTES);
       tma_load_tile<D>(smem + C::OFF_Q, &tm_q, &sh.q_full, row0, bh);
       if (rows_b > 0)
@@ -163,29 +166,34 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
         tma_load_tile<D>(smem + C::OFF_K + ks * C::TILE_BYTES, &tm_k, &sh.k_full[ks], j * kTileRows, bh);
+      }
+      if (!ok) {
+        // Drain every copy that may still be in flight (Q and the last NK K tiles).
+        mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
+        for (int jj = max(0, j - C::NK); jj < j; ++jj)
+          mbar_wait_drain(&sh.k_full[jj % C::NK], (jj / C::NK) & 1, a.timeout_ns);
+      }
+      if (a.tile_count != nullptr) {
+        const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        a.tile_count[cta] = j;
+      }
+    } else if (warp == 3 && lane == 0) {
+      // ---------------- TMA producer: the V ring ----------------
+      tma_prefetch_desc(&tm_v);
+      int j = 0;
+      bool ok = true;
+      for (; j < n_total && ok; ++j) {
         const int vs = j % C::NV, vp = (j / C::NV) & 1;
         ok = mbar_wait(&sh.v_empty[vs], vp ^ 1, wc);
-        if (!ok) {
-          // K_j is in flight: let it land before leaving.
-          mbar_wait_drain(&sh.k_full[ks], kp, a.timeout_ns);
-          break;
-        }
+        if (!ok) break;
         if (a.fault == 1 && j == 0) continue;  // failure-path test: V_0 never arrives
         mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
         tma_load_tile<D>(smem + C::OFF_V + vs * C::TILE_BYTES, &tm_v, &sh.v_full[vs], j * kTileRows, bh);
       }
       if (!ok) {
-        // Drain every copy that may still be in flight (the last NK/NV issued).
-        mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
-        for (int jj = max(0, j - C::NK); jj < j; ++jj)
-          mbar_wait_drain(&sh.k_full[jj % C::NK], (jj / C::NK) & 1, a.timeout_ns);
         for (int jj = max(0, j - C::NV); jj < j; ++jj)
           if (!(a.fault == 1 && jj == 0))
             mbar_wait_drain(&sh.v_full[jj % C::NV], (jj / C::NV) & 1, a.timeout_ns);
-      }
-      if (a.tile_count != nullptr) {
-        const int cta = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        a.tile_count[cta] = j;
       }
     } else if (warp == 1) {
       // ---------------- tcgen05.mma issuer (the whole warp; one lane issues) ----------------
@@ -206,13 +214,10 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int j = 0; j < n_total && ok; ++j) {
         const bool more = (j + 1 < n_total);
-        if (more) {
-          const int ks = (j + 1) % C::NK;
-          ok = mbar_wait_warp(&sh.k_full[ks], ((j + 1) / C::NK) & 1, wc);
-          if (!ok) break;
-        }
-        const int vs = j % C::NV;
-        ok = mbar_wait_warp(&sh.v_full[vs], (j / C::NV) & 1, wc);
+        const int ks = (j + 1) % C::NK, vs = j % C::NV;
+        ok = more ? mbar_wait2_warp(&sh.k_full[ks], ((j + 1) / C::NK) & 1, &sh.v_full[vs],
+                                    (j / C::NV) & 1, wc)
+                  : mbar_wait_warp(&sh.v_full[vs], (j / C::NV) & 1, wc);
         if (!ok) break;
         const uint32_t v_smem = smem_u32(smem + C::OFF_V + vs * C::TILE_BYTES);
         const uint32_t k_next = smem_u32(smem + C::OFF_K + ((j + 1) % C::NK) * C::TILE_BYTES);
@@ -275,16 +280,18 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) s[c] = __float_as_uint(-INFINITY);
       }
-      // Row max as a tree of independent maxima (short dependency chains).
+      // Row max as eight independent chains of three-input maxima (short
+      // dependency chains, half the instructions of two-input maxima).
       float mx8[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = __uint_as_float(s[u]);
+      for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(__uint_as_float(s[u]), __uint_as_float(s[8 + u]));
 #pragma unroll
-      for (int c = 8; c < 128; c += 8)
+      for (int c = 16; c < 128; c += 16)
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(mx8[u], __uint_as_float(s[c + u]));
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        for (int u = 0; u < 8; ++u)
+          mx8[u] = fmax3(mx8[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
+      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                             fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
       const float m_new = fmaxf(m_ref, mx);
       const bool rescale = (m_new - m_ref) * sl2 > kRescaleLog2;  // also true when m_ref = -inf
       float alpha = 1.f;
