@@ -99,54 +99,70 @@ struct BwdQShared {
 // 1. preprocess
 // ---------------------------------------------------------------------------
 template <int D, bool BF16>
+__device__ __forceinline__ float dot8(uint4 x, uint4 y) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    float x0, x1, y0, y1;
+    if constexpr (BF16) {
+      x0 = __uint_as_float(xs[w] << 16); x1 = __uint_as_float(xs[w] & 0xffff0000u);
+      y0 = __uint_as_float(ys[w] << 16); y1 = __uint_as_float(ys[w] & 0xffff0000u);
+    } else {
+      const __half2 xh = *reinterpret_cast<const __half2*>(&xs[w]);
+      const __half2 yh = *reinterpret_cast<const __half2*>(&ys[w]);
+      x0 = __low2float(xh); x1 = __high2float(xh);
+      y0 = __low2float(yh); y1 = __high2float(yh);
+    }
+    acc = fmaf(x0, y0, acc);
+    acc = fmaf(x1, y1, acc);
+  }
+  return acc;
+}
+
+// One row is D/8 lanes of 16 bytes, so a warp covers 32/(D/8) rows per pass,
+// and each warp keeps kPrePasses passes of loads in flight before reducing.
+constexpr int kPrePasses = 4;
+
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
     fa2_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ dsum_pad,
                        float* __restrict__ l2_pad, int BH, int N, int n_pad) {
-  constexpr int EPL = D / 32;  // elements per lane: 4 (d=128) or 2 (d=64)
-  const int lane = threadIdx.x & 31;
+  constexpr int LPR = D / 8;     // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp per pass
+  constexpr int U = kPrePasses;
+  const int lane = threadIdx.x & 31, sub = lane / LPR, li = lane % LPR;
   const long long total = static_cast<long long>(BH) * n_pad;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < total; r += warps) {
-    const int bh = static_cast<int>(r / n_pad), i = static_cast<int>(r % n_pad);
-    float dsum = 0.f, l2 = 0.f;
-    if (i < N) {
-      const size_t row = static_cast<size_t>(bh) * N + i;
-      const uint16_t* po = o + row * D + lane * EPL;
-      const uint16_t* pd = dout + row * D + lane * EPL;
-      uint32_t ow[EPL / 2], dw[EPL / 2];
-      if constexpr (EPL == 4) {
-        const uint2 x = *reinterpret_cast<const uint2*>(po);
-        const uint2 y = *reinterpret_cast<const uint2*>(pd);
-        ow[0] = x.x; ow[1] = x.y; dw[0] = y.x; dw[1] = y.y;
-      } else {
-        ow[0] = *reinterpret_cast<const uint32_t*>(po);
-        dw[0] = *reinterpret_cast<const uint32_t*>(pd);
-      }
-      float acc = 0.f;
+  const long long warp_id = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long stride = static_cast<long long>(gridDim.x) * (blockDim.x >> 5) * RPW * U;
+  for (long long base = warp_id * RPW * U; base < total; base += stride) {
+    uint4 ov[U], dv[U];
+    bool valid[U];
+    size_t src[U];
 #pragma unroll
-      for (int w = 0; w < EPL / 2; ++w) {
-        float o0, o1, d0, d1;
-        if constexpr (BF16) {
-          o0 = __uint_as_float(ow[w] << 16); o1 = __uint_as_float(ow[w] & 0xffff0000u);
-          d0 = __uint_as_float(dw[w] << 16); d1 = __uint_as_float(dw[w] & 0xffff0000u);
-        } else {
-          const __half2 oh = *reinterpret_cast<const __half2*>(&ow[w]);
-          const __half2 dh = *reinterpret_cast<const __half2*>(&dw[w]);
-          o0 = __low2float(oh); o1 = __high2float(oh);
-          d0 = __low2float(dh); d1 = __high2float(dh);
-        }
-        acc = fmaf(o0, d0, acc);
-        acc = fmaf(o1, d1, acc);
+    for (int u = 0; u < U; ++u) {
+      const long long r = base + u * RPW + sub;
+      const int bh = static_cast<int>(r / n_pad), i = static_cast<int>(r % n_pad);
+      valid[u] = r < total && i < N;
+      src[u] = valid[u] ? static_cast<size_t>(bh) * N + i : 0;
+      ov[u] = make_uint4(0u, 0u, 0u, 0u);
+      dv[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (valid[u]) {
+        ov[u] = *reinterpret_cast<const uint4*>(o + src[u] * D + li * 8);
+        dv[u] = *reinterpret_cast<const uint4*>(dout + src[u] * D + li * 8);
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-      dsum = acc;
-      l2 = lse[row] * kLog2e;
     }
-    if (lane == 0) {
-      dsum_pad[r] = dsum;
-      l2_pad[r] = l2;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float acc = dot8<D, BF16>(ov[u], dv[u]);
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const long long r = base + u * RPW + sub;
+      if (li == 0 && r < total) {
+        dsum_pad[r] = valid[u] ? acc : 0.f;
+        l2_pad[r] = valid[u] ? lse[src[u]] * kLog2e : 0.f;
+      }
     }
   }
 }
@@ -757,8 +773,9 @@ static cudaError_t launch_bwd_t(const void* o, const void* dO, const float* lse,
   if (ev) cudaEventRecord(ev[0], stream);
   {
     const long long rows = static_cast<long long>(BH) * a.n_pad;
-    long long blocks = (rows + 7) / 8;
-    const long long cap = static_cast<long long>(g_num_sms) * 16;
+    const long long rows_per_block = 8LL * (32 / (D / 8)) * kPrePasses;  // 8 warps
+    long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+    const long long cap = static_cast<long long>(g_num_sms) * 8;
     if (blocks > cap) blocks = cap;
     fa2_bwd_pre_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, stream>>>(
         static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, dsum, l2, BH,
