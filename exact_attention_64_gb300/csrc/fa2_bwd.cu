@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(384, 1)
         const float4 l4 = reinterpret_cast<const float4*>(ld_s)[u];
         lreg[4 * u] = l4.x; lreg[4 * u + 1] = l4.y; lreg[4 * u + 2] = l4.z; lreg[4 * u + 3] = l4.w;
       }
-      ok = mbar_wait(&sh.st_full, i & 1, wc);
+      ok = mbar_wait_warp(&sh.st_full, i & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(384, 1)
         dreg[4 * u] = d4.x; dreg[4 * u + 1] = d4.y; dreg[4 * u + 2] = d4.z; dreg[4 * u + 3] = d4.w;
       }
 
-      ok = mbar_wait(&sh.dpt_full, i & 1, wc);
+      ok = mbar_wait_warp(&sh.dpt_full, i & 1, wc);
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
     // ---------------- epilogue: dV, scale*dK -> 16-bit, TMA store ----------------
-    if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
+    if (ok) ok = mbar_wait_warp(&sh.mma_done, 0, wc);
     // All MMAs have completed, so the K and V buffers are free for staging.
     uint8_t* stage = smem + (wg == 0 ? C::OFF_FIX1 : C::OFF_FIX0);
     if (ok) {
@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(384, 1)
     for (int j = 0; j < n_kv; ++j) {
       const int b = j & 1;
       const int kc0 = j * kTileRows + 64 * wg;  // first key column of this warpgroup
-      ok = mbar_wait(&sh.st_full, j & 1, wc);
+      ok = mbar_wait_warp(&sh.st_full, j & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
@@ -728,7 +728,7 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) mbar_arrive(&sh.ds_full);
     }
     // ---------------- epilogue: scale * dQ -> 16-bit, TMA store ----------------
-    if (ok) ok = mbar_wait(&sh.mma_done, 0, wc);
+    if (ok) ok = mbar_wait_warp(&sh.mma_done, 0, wc);
     // Every MMA has completed: the Q buffer is free for staging.
     uint8_t* stage = smem + Q::OFF_Q;
     if (ok && wg == 0) {

@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(384, 1)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = mbar_wait(&sh.s_full[t], j & 1, wc);
+      ok = mbar_wait_warp(&sh.s_full[t], j & 1, wc);
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_st();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O_t still holds the sum up to tile j-1: wait for that product, then rescale.
-        ok = mbar_wait(&sh.o_full[t], (j - 1) & 1, wc);
+        ok = mbar_wait_warp(&sh.o_full[t], (j - 1) & 1, wc);
         if (!ok) break;
         __syncwarp();
         tc_fence_after();
@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) mbar_arrive(&sh.p_full[t]);
     }
     // ---------------- epilogue: O / l -> 16-bit, L = m + ln l ----------------
-    if (ok && nt > 0) ok = mbar_wait(&sh.o_full[t], (nt - 1) & 1, wc);
+    if (ok && nt > 0) ok = mbar_wait_warp(&sh.o_full[t], (nt - 1) & 1, wc);
     // Q_t's shared buffer is free (its last S product has completed): stage O
     // there in the same 128-byte-swizzled layout and store it with TMA, which
     // also clips rows past the sequence end.
