@@ -13,6 +13,17 @@ the matching section of "大猿搬砖简记"): one worker per K/V column block, 
 dK and dV accumulate along the query direction and only dQ accumulates along
 the key direction.
 
+KV split ("大猿搬砖简记", thread-block section; the num_splits_heuristic_fwd
+paragraph): when the (row block, batch, head) workers cannot fill the SMs, the
+K/V range of each worker may be cut into num_splits parts whose partial results
+are merged afterwards. The split count is chosen by computing the SM
+utilisation of each candidate, taking the best, and picking the smallest
+candidate whose utilisation is at least 0.95 of it. The page does not define
+the utilisation; reading: with w = workers * s / num_sms waves, utilisation is
+w / ceil(w), the filled fraction of the waves launched. Candidates run from 1
+to min(max_splits, num_sms, number of K/V tiles): more parts than K/V tiles
+leave parts empty, more than the SM count add no wave.
+
 Causal tile skipping ("flash-attention123和ring-attention", 优化3): key/query
 tile pairs that the causal mask hides completely are dropped, not computed.
 Reading (the first two pages say such tiles are still loaded; the third says
@@ -29,6 +40,9 @@ __all__ = [
     "fwd_kv_tile_range",
     "bwd_grid",
     "bwd_q_tile_range",
+    "split_utilisation",
+    "num_splits_heuristic",
+    "split_kv_range",
 ]
 
 
@@ -91,3 +105,33 @@ def bwd_q_tile_range(n_block: int, N: int, block_m: int, block_n: int, causal: b
         return (0, 0)
     assert visited == list(range(visited[0], visited[-1] + 1))
     return (visited[0], visited[-1] + 1)
+
+
+def split_utilisation(workers: int, num_sms: int, s: int) -> float:
+    """Filled fraction of the waves when `workers` workers are each cut into
+    `s` parts on `num_sms` SMs (the reading of the page's "SM utilisation")."""
+    waves = workers * s / num_sms
+    return waves / ceil_div(workers * s, num_sms)
+
+
+def num_splits_heuristic(workers: int, num_sms: int, num_n_blocks: int, max_splits: int) -> int:
+    """The page's rule: best utilisation over the candidates, then the smallest
+    candidate whose utilisation is >= 0.95 of the best."""
+    top = max(1, min(max_splits, num_sms, num_n_blocks))
+    eff = [split_utilisation(workers, num_sms, s) for s in range(1, top + 1)]
+    best = max(eff)
+    for s in range(1, top + 1):
+        if eff[s - 1] >= 0.95 * best:
+            return s
+    return 1
+
+
+def split_kv_range(j_begin: int, j_end: int, num_splits: int, split: int):
+    """Part `split` of a worker's K/V tile range [j_begin, j_end) cut into
+    `num_splits` contiguous parts of ceil(len / num_splits) tiles each (the
+    last parts shorter or empty)."""
+    n = max(0, j_end - j_begin)
+    per = ceil_div(n, num_splits) if n else 0
+    lo = min(j_begin + split * per, j_end) if n else j_begin
+    hi = min(lo + per, j_end) if n else j_begin
+    return (lo, hi)

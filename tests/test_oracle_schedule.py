@@ -56,3 +56,56 @@ def test_causal_skips_about_half_the_tiles():
     nb = N // bm
     assert full == nb * nb
     assert causal == nb * (nb + 1) // 2
+
+
+# ---- KV split ("大猿搬砖简记", thread-block section: num_splits_heuristic_fwd) ----
+
+def test_split_utilisation_closed_forms():
+    # One full wave, a partial wave, and a wave and a third.
+    assert schedule.split_utilisation(152, 152, 1) == 1.0
+    assert schedule.split_utilisation(128, 152, 1) == pytest.approx(128 / 152)
+    assert schedule.split_utilisation(100, 152, 2) == pytest.approx(200 / 152 / 2)
+    assert schedule.split_utilisation(76, 152, 4) == 1.0
+
+
+def test_num_splits_worked_by_hand():
+    """128 workers (2 heads x 64 row blocks of 256) on 152 SMs, 128 K/V tiles.
+    Utilisation of s parts is (16s/19) / ceil(16s/19): 16/19 = 0.842 for
+    s = 1..6 (16s/19 = 0.84, 1.68, 2.53, 3.37, 4.21, 5.05), 112/114 = 0.982
+    for s = 7, and 1 at s = 19 (16 full waves). The best is 1; the smallest
+    s reaching 0.95 of it is 7."""
+    assert schedule.num_splits_heuristic(128, 152, 128, 128) == 7
+
+
+def test_num_splits_is_one_when_the_grid_fills_whole_waves():
+    for k in (1, 2, 5):
+        assert schedule.num_splits_heuristic(152 * k, 152, 64, 128) == 1
+
+
+def test_num_splits_capped_by_tiles_and_max():
+    # Two K/V tiles: at most two parts, whatever the fill.
+    assert schedule.num_splits_heuristic(1, 152, 2, 128) <= 2
+    assert schedule.num_splits_heuristic(3, 152, 100, 4) <= 4
+
+
+def test_num_splits_follows_the_stated_rule():
+    """The choice has utilisation >= 0.95 of the best candidate and no smaller
+    candidate has (the page's selection rule, checked over a sweep)."""
+    for workers in (1, 3, 17, 64, 128, 151, 153, 300):
+        for nb in (1, 2, 7, 64, 128):
+            s = schedule.num_splits_heuristic(workers, 152, nb, 128)
+            top = min(128, 152, nb)
+            eff = [schedule.split_utilisation(workers, 152, c) for c in range(1, top + 1)]
+            assert eff[s - 1] >= 0.95 * max(eff)
+            assert all(eff[c - 1] < 0.95 * max(eff) for c in range(1, s))
+
+
+@pytest.mark.parametrize("j0,j1", [(0, 0), (0, 1), (0, 5), (3, 17), (0, 128)])
+def test_split_kv_range_partitions_the_range(j0, j1):
+    for S in range(1, 9):
+        parts = [schedule.split_kv_range(j0, j1, S, s) for s in range(S)]
+        covered = [j for lo, hi in parts for j in range(lo, hi)]
+        assert covered == list(range(j0, j1))  # disjoint, in order, complete
+        per = schedule.ceil_div(j1 - j0, S) if j1 > j0 else 0
+        assert all(hi - lo <= per for lo, hi in parts)
+        assert all(j0 <= lo <= hi <= j1 for lo, hi in parts)
