@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-heads", type=int, default=3)
+    p.add_argument("--fwd-splits", default="1",
+                   help="K/V parts per forward worker: an integer or 'auto' (fa2_fwd_split)")
     return p.parse_args()
 
 
@@ -232,9 +234,22 @@ def main():
     scale = w.scale
     causal = int(w.causal)
 
+    if args.fwd_splits == "auto":
+        fwd_splits = fa2.num_splits(B, H, N, d, bool(causal),
+                                    torch.cuda.get_device_properties(dev).multi_processor_count)
+    else:
+        fwd_splits = int(args.fwd_splits)
+    split_bytes = lib.fa2_fwd_split_workspace_size(B, H, N, d, fwd_splits) if fwd_splits > 1 else 0
+    split_ws = torch.empty(max(split_bytes, 1), dtype=torch.uint8, device=dev)
+
     def fwd():
-        c = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H,
-                        N, d, causal, scale, dt_code, sp)
+        if fwd_splits > 1:
+            c = lib.fa2_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), B, H, N, d, causal, scale, dt_code, fwd_splits,
+                                  split_ws.data_ptr(), split_bytes, sp)
+        else:
+            c = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, N, d, causal, scale, dt_code, sp)
         if c:
             raise fa2.FA2Error("fa2_fwd", c)
 
@@ -376,7 +391,7 @@ def main():
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "q_std": w.q_std, "parallelism": f"head-sharded replicas x{world}",
                    "l2": f"inputs larger than L2 ({step_bytes / 2**20:.0f} MiB touched per step "
-                         f"> {L2_BYTES / 2**20:.0f} MiB)"},
+                         f"> {L2_BYTES / 2**20:.0f} MiB)", "fwd_splits": fwd_splits},
         "detail": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
                    "fwd_frac_of_peak": fwd_tf / pk["bf16_sustained"],
                    "bwd_frac_of_peak": bwd_tf / pk["bf16_sustained"],
@@ -384,7 +399,7 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": (5 if fwd_splits > 1 else 4) * args.steps,  # + the merge pass when split
         "clocks": clk.summary(),
     }
     if rank == 0:

@@ -67,6 +67,9 @@ def load_library() -> ctypes.CDLL:
     sigs = {
         "fa2_fwd": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
         "fa2_fwd_instrumented": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]),
+        "fa2_fwd_split": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]),
+        "fa2_fwd_split_workspace_size": (sz, [i, i, i, i, i]),
+        "fa2_num_splits": (i, [i, i, i, i, i, i]),
         "fa2_bwd_workspace_size": (sz, [i, i, i, i]),
         "fa2_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]),
         "fa2_bwd_timed": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp,
@@ -119,10 +122,20 @@ def _check_tensor(name, t, shape, dtype, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+def num_splits(B: int, H: int, N: int, d: int, causal: bool, num_sms: int) -> int:
+    """The K/V split count ``fa2_fwd_split`` would use for this shape on a GPU
+    with ``num_sms`` SMs (host-only rule of the library)."""
+    return int(load_library().fa2_num_splits(B, H, N, d, int(bool(causal)), num_sms))
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            num_splits: int | str = 1):
     """O = softmax(scale * Q K^T [+ causal mask]) V and its logsumexp L.
 
-    Returns (o, lse): o like q, lse float32 [B, H, N] (natural log).
+    ``num_splits`` > 1 cuts each worker's K/V range into that many parts run by
+    separate CTAs and merges them (fa2_fwd_split); "auto" picks the count with
+    the library's rule for this GPU. Returns (o, lse): o like q, lse float32
+    [B, H, N] (natural log).
     """
     B, H, N, d = _shape(q)
     dt = q.dtype
@@ -140,6 +153,20 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     _check_tensor("out", out, (B, H, N, d), dt, dev)
     _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
     lib = load_library()
+    if num_splits == "auto":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        num_splits = int(lib.fa2_num_splits(B, H, N, d, int(bool(causal)), sms))
+    num_splits = int(num_splits)
+    if num_splits > 1:
+        nbytes = lib.fa2_fwd_split_workspace_size(B, H, N, d, num_splits)
+        if nbytes == 0:
+            raise FA2Error("fa2_fwd_split_workspace_size", 1)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        code = lib.fa2_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                 _DTYPES[dt], num_splits, ws.data_ptr(), nbytes, _stream_ptr(dev))
+        _check("fa2_fwd_split", code)
+        return out, lse
     code = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, d, int(bool(causal)), float(scale), _DTYPES[dt], _stream_ptr(dev))
     _check("fa2_fwd", code)

@@ -15,6 +15,8 @@ namespace fa2 {
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
                        cudaStream_t stream);
+cudaError_t launch_fwd_combine(int d, bool bf16, const float* o_part, const float* lse_part, void* o,
+                               float* lse, int S, long long rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd(int d, bool bf16, bool causal, const void* o, const void* dO,
                        const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
                        float* l2, cudaStream_t stream, cudaEvent_t* ev);
@@ -27,6 +29,7 @@ namespace {
 __device__ int g_device_status;
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxFwdSplits = 128;  // largest K/V split count fa2_fwd_split accepts
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -135,7 +138,8 @@ int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dt
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-             int d, int causal, float scale, int dtype, int* tile_counts, void* stream) {
+             int d, int causal, float scale, int dtype, int* tile_counts, void* stream,
+             int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
   int st = check_common(B, H, N, d, causal, scale, dtype);
   if (st != FA2_OK) return st;
@@ -147,11 +151,25 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   for (const void* in : ins)
     if (overlap(o, tbytes, in, tbytes) || overlap(lse, lbytes, in, tbytes)) return FA2_ERR_OVERLAP;
   if (overlap(o, tbytes, lse, lbytes)) return FA2_ERR_OVERLAP;
+  const int BH = B * H;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (num_splits > 1) {
+    const size_t need = fa2_fwd_split_workspace_size(B, H, N, d, num_splits);
+    if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return FA2_ERR_ALIGNMENT;
+    for (const void* in : ins)
+      if (overlap(workspace, need, in, tbytes)) return FA2_ERR_OVERLAP;
+    if (overlap(workspace, need, o, tbytes) || overlap(workspace, need, lse, lbytes))
+      return FA2_ERR_OVERLAP;
+    o_part = static_cast<float*>(workspace);
+    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                        align_up(static_cast<size_t>(num_splits) * BH * N * d * 4, 256));
+  }
   int dev = 0;
   int* status = nullptr;
   st = device_setup(&dev, &status);
   if (st != FA2_OK) return st;
-  const int BH = B * H;
   CUtensorMap tq, tk, tv, to;
   if (make_map_16bit(&tq, q, BH, N, d, dtype) || make_map_16bit(&tk, k, BH, N, d, dtype) ||
       make_map_16bit(&tv, v, BH, N, d, dtype) || make_map_16bit(&to, o, BH, N, d, dtype))
@@ -167,7 +185,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.tile_count = tile_counts;
   a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
   a.fault = 0;
-  {
+  a.num_splits = num_splits;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  if (num_splits <= 1) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_fault_kind != 0) {
       a.fault = g_fault_kind;
@@ -178,8 +199,14 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // A non-sticky error left in this thread by another caller would otherwise be
   // reported as ours by the post-launch check.
   (void)cudaGetLastError();
-  const cudaError_t e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
-                                        static_cast<cudaStream_t>(stream));
+  cudaError_t e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
+                                  static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess && num_splits > 1) {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    e = fa2::launch_fwd_combine(d, dtype == FA2_BF16, o_part, lse_part, o, lse, num_splits,
+                                static_cast<long long>(BH) * N, sms, static_cast<cudaStream_t>(stream));
+  }
   return e == cudaSuccess ? FA2_OK : cuda_fail(e);
 }
 
@@ -190,6 +217,31 @@ extern "C" {
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
             int d, int causal, float scale, int dtype, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, nullptr, stream);
+}
+
+size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || num_splits < 1 ||
+      num_splits > kMaxFwdSplits)
+    return 0;
+  // [O parts: num_splits x B*H x N x d fp32][lse parts: num_splits x B*H x N fp32]
+  const size_t rows = static_cast<size_t>(num_splits) * B * H * N;
+  return align_up(rows * d * 4, 256) + align_up(rows * 4, 256);
+}
+
+int fa2_num_splits(int B, int H, int N, int d, int causal, int num_sms) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1) ||
+      num_sms < 1)
+    return 0;
+  const int workers = B * H * fa2::fwd_num_m_blocks(N);
+  return fa2::fwd_num_splits(workers, num_sms, fa2::ceil_div(N, fa2::kTileRows), kMaxFwdSplits);
+}
+
+int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int N, int d, int causal, float scale, int dtype, int num_splits, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (num_splits < 1 || num_splits > kMaxFwdSplits) return FA2_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, nullptr, stream, num_splits,
+                  workspace, workspace_bytes);
 }
 
 int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -37,6 +37,39 @@ __host__ __device__ inline int fwd_kv_tile_end(int row_begin, int row_end, int N
   return causal ? ceil_div(row_end, kTileRows) : ceil_div(N, kTileRows);
 }
 
+// KV split ("大猿搬砖简记", thread-block section, the num_splits_heuristic_fwd
+// paragraph). When the (row block, batch, head) workers cannot fill the SMs,
+// each worker's K/V tile range [0, end) is cut into num_splits contiguous parts
+// of ceil(end / num_splits) tiles (the last parts shorter or empty); part s is
+// [lo, hi). The partial results are merged by the online-softmax rule.
+__host__ __device__ inline void fwd_split_range(int end, int num_splits, int split, int* lo, int* hi) {
+  const int per = end > 0 ? ceil_div(end, num_splits) : 0;
+  *lo = min(split * per, end);
+  *hi = min(*lo + per, end);
+}
+
+// The split count: for each candidate s in [1, min(max_splits, num_sms,
+// num_n_blocks)], the SM utilisation is w / ceil(w) with w = workers * s /
+// num_sms waves (the filled fraction of the waves; the page does not define
+// it); take the best and return the smallest s within 0.95 of it.
+inline int fwd_num_splits(int workers, int num_sms, int num_n_blocks, int max_splits) {
+  int top = max_splits < num_sms ? max_splits : num_sms;
+  if (num_n_blocks < top) top = num_n_blocks;
+  if (top < 1) top = 1;
+  double best = 0.0;
+  for (int s = 1; s <= top; ++s) {
+    const long long cells = static_cast<long long>(workers) * s;
+    const double eff = (static_cast<double>(cells) / num_sms) / static_cast<double>((cells + num_sms - 1) / num_sms);
+    if (eff > best) best = eff;
+  }
+  for (int s = 1; s <= top; ++s) {
+    const long long cells = static_cast<long long>(workers) * s;
+    const double eff = (static_cast<double>(cells) / num_sms) / static_cast<double>((cells + num_sms - 1) / num_sms);
+    if (eff >= 0.95 * best) return s;
+  }
+  return 1;
+}
+
 // Backward work mapping. dK and dV accumulate along the query direction, so
 // their worker owns a K/V column block ("FlashAttention学习笔记(2)",
 // Foward和backward中的thread block划分): one CTA per 128-key block, the column
@@ -67,6 +100,9 @@ struct FwdArgs {
   int* tile_count;    // optional: per-CTA count of K/V tiles loaded (nullptr = off)
   unsigned long long timeout_ns;  // bound on every mbarrier wait
   int fault;          // 0 normally; 1 = producer skips the first V tile (failure-path test)
+  int num_splits;     // K/V parts per worker; <= 1: no split
+  float* o_part;      // split mode: [num_splits][B*H][N][d] fp32 O / l of each part
+  float* lse_part;    // split mode: [num_splits][B*H][N] fp32 logsumexp of each part (-inf: empty)
 };
 
 struct BwdArgs {

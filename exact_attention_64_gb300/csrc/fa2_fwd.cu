@@ -113,13 +113,22 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
-  const int mb = fwd_m_block_of(blockIdx.x, a.num_m_blocks, CAUSAL);
-  const int bh = blockIdx.y * a.H + blockIdx.z;  // grid = (m block, batch, head)
+  // grid = (m block x K/V part, batch, head); without a split there is one part.
+  const int S = a.num_splits > 1 ? a.num_splits : 1;
+  const int split = blockIdx.x % S;
+  const int mb = fwd_m_block_of(blockIdx.x / S, a.num_m_blocks, CAUSAL);
+  const int bh = blockIdx.y * a.H + blockIdx.z;
   const int row0 = mb * kFwdRowsPerCta;
   const int rows_a = min(kTileRows, N - row0);
   const int rows_b = max(0, min(kTileRows, N - row0 - kTileRows));
-  const int n_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, N, CAUSAL),
-                      fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, N, CAUSAL)};
+  const int end_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, N, CAUSAL),
+                        fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, N, CAUSAL)};
+  // This CTA's part [kv_lo, kv_hi) of the K/V tiles. Below, j counts tiles
+  // within the part (ring slots, phases, first-tile flags); kv_lo + j is the
+  // K/V tile itself (TMA coordinates, masks).
+  int kv_lo, kv_hi;
+  fwd_split_range(max(end_t[0], end_t[1]), S, split, &kv_lo, &kv_hi);
+  const int n_t[2] = {max(0, min(kv_hi, end_t[0]) - kv_lo), max(0, min(kv_hi, end_t[1]) - kv_lo)};
   const int n_total = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
@@ -154,10 +163,12 @@ __global__ void __launch_bounds__(384, 1)
       // (V_j is read by the last products of step j) never holds up K_{j+1}.
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(&sh.q_full, (rows_b > 0 ? 2 : 1) * C::TILE_BYTES);
-      tma_load_tile<D>(smem + C::OFF_Q, &tm_q, &sh.q_full, row0, bh);
-      if (rows_b > 0)
-        tma_load_tile<D>(smem + C::OFF_Q + C::TILE_BYTES, &tm_q, &sh.q_full, row0 + kTileRows, bh);
+      if (n_total > 0) {  // an empty part loads nothing
+        mbar_arrive_expect_tx(&sh.q_full, (rows_b > 0 ? 2 : 1) * C::TILE_BYTES);
+        tma_load_tile<D>(smem + C::OFF_Q, &tm_q, &sh.q_full, row0, bh);
+        if (rows_b > 0)
+          tma_load_tile<D>(smem + C::OFF_Q + C::TILE_BYTES, &tm_q, &sh.q_full, row0 + kTileRows, bh);
+      }
       int j = 0;
       bool ok = true;
       for (; j < n_total && ok; ++j) {
@@ -165,11 +176,12 @@ __global__ void __launch_bounds__(384, 1)
         ok = mbar_wait(&sh.k_empty[ks], kp ^ 1, wc);
         if (!ok) break;
         mbar_arrive_expect_tx(&sh.k_full[ks], C::TILE_BYTES);
-        tma_load_tile<D>(smem + C::OFF_K + ks * C::TILE_BYTES, &tm_k, &sh.k_full[ks], j * kTileRows, bh);
+        tma_load_tile<D>(smem + C::OFF_K + ks * C::TILE_BYTES, &tm_k, &sh.k_full[ks],
+                         (kv_lo + j) * kTileRows, bh);
       }
       if (!ok) {
         // Drain every copy that may still be in flight (Q and the last NK K tiles).
-        mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
+        if (n_total > 0) mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
         for (int jj = max(0, j - C::NK); jj < j; ++jj)
           mbar_wait_drain(&sh.k_full[jj % C::NK], (jj / C::NK) & 1, a.timeout_ns);
       }
@@ -188,7 +200,8 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         if (a.fault == 1 && j == 0) continue;  // failure-path test: V_0 never arrives
         mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
-        tma_load_tile<D>(smem + C::OFF_V + vs * C::TILE_BYTES, &tm_v, &sh.v_full[vs], j * kTileRows, bh);
+        tma_load_tile<D>(smem + C::OFF_V + vs * C::TILE_BYTES, &tm_v, &sh.v_full[vs],
+                         (kv_lo + j) * kTileRows, bh);
       }
       if (!ok) {
         for (int jj = max(0, j - C::NV); jj < j; ++jj)
@@ -198,9 +211,9 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 1) {
       // ---------------- tcgen05.mma issuer (the whole warp; one lane issues) ----------------
       const uint32_t q_s[2] = {smem_u32(smem + C::OFF_Q), smem_u32(smem + C::OFF_Q + C::TILE_BYTES)};
-      bool ok = mbar_wait_warp(&sh.q_full, 0, wc);
-      ok = ok && mbar_wait_warp(&sh.k_full[0], 0, wc);
-      if (ok) {
+      // An empty part (n_total == 0) has nothing to wait for or issue.
+      bool ok = n_total == 0 || (mbar_wait_warp(&sh.q_full, 0, wc) && mbar_wait_warp(&sh.k_full[0], 0, wc));
+      if (ok && n_total > 0) {
         tc_fence_after();
         const uint32_t k0 = smem_u32(smem + C::OFF_K);
 #pragma unroll
@@ -272,7 +285,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_wait_ld();
       reg_fence(s);
       // Mask keys past the sequence end and, on the diagonal tile, keys after the query.
-      const int kv0 = j * kTileRows;
+      const int kv0 = (kv_lo + j) * kTileRows;
       const bool need_mask = (kv0 + kTileRows > N) || (CAUSAL && kv0 + kTileRows - 1 > row_base);
       if (need_mask) {
         const int lim = CAUSAL ? min(N - kv0, my_row - kv0 + 1) : (N - kv0);
@@ -343,44 +356,79 @@ __global__ void __launch_bounds__(384, 1)
     }
     // ---------------- epilogue: O / l -> 16-bit, L = m + ln l ----------------
     if (ok && nt > 0) ok = mbar_wait_warp(&sh.o_full[t], (nt - 1) & 1, wc);
-    // Q_t's shared buffer is free (its last S product has completed): stage O
-    // there in the same 128-byte-swizzled layout and store it with TMA, which
-    // also clips rows past the sequence end.
-    uint8_t* stage = smem + C::OFF_Q + t * C::TILE_BYTES;
-    if (ok && nt > 0) {
-      __syncwarp();
-      tc_fence_after();
-      const float inv_l = 1.f / l;
+    if (a.o_part != nullptr) {
+      // K/V split: this part's O / l in fp32 and its logsumexp, for the merge
+      // pass; an empty part contributes O = 0 with logsumexp -inf. The TMEM
+      // loads are warp-collective: the whole warp runs them, and only the
+      // stores are limited to rows inside the sequence.
+      const bool row_in = my_row < N;
+      const size_t prow = static_cast<size_t>(split) * (static_cast<size_t>(a.B) * a.H) * N +
+                          static_cast<size_t>(bh) * N + (row_in ? my_row : 0);
+      float4* dst = reinterpret_cast<float4*>(a.o_part + prow * D);
+      if (ok && nt > 0) {
+        __syncwarp();
+        tc_fence_after();
+        const float inv_l = 1.f / l;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(t_o + c, o);
-        tmem_wait_ld();
-        reg_fence(o);
-        const int slab = c / 64;
-        const int chunk0 = (c % 64) / 8;
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          if (row_in) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 val;
-          val.x = pack_x2<BF16>(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
-          val.y = pack_x2<BF16>(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
-          val.z = pack_x2<BF16>(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
-          val.w = pack_x2<BF16>(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
-          const int phys = (chunk0 + k) ^ (r & 7);
-          *reinterpret_cast<uint4*>(stage + slab * C::SLAB_BYTES + r * 128 + phys * 16) = val;
+            for (int k = 0; k < 8; ++k)
+              dst[c / 4 + k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                                           __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+          }
         }
-      }
-      fence_proxy_async_smem();
-      if (my_row < N) a.lse[static_cast<size_t>(bh) * N + my_row] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
-    }
-    // Every warp of the group reaches this barrier on every path, aborted or not.
-    named_bar_sync(1 + t, 128);
-    if ((threadIdx.x & 127) == 0 && nt > 0 && *abort_flag == 0) {
+        if (row_in) a.lse_part[prow] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
+      } else if (ok && row_in) {
 #pragma unroll
-      for (int s = 0; s < D / 64; ++s)
-        tma_store_3d(&tm_o, stage + s * C::SLAB_BYTES, s * 64, row_base, bh);
-      bulk_commit_group();
-      bulk_wait_group_read0();
+        for (int k = 0; k < D / 4; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        a.lse_part[prow] = -INFINITY;
+      }
+      named_bar_sync(1 + t, 128);  // as below: every warp of the group reaches it
+    } else {
+      // Q_t's shared buffer is free (its last S product has completed): stage O
+      // there in the same 128-byte-swizzled layout and store it with TMA, which
+      // also clips rows past the sequence end.
+      uint8_t* stage = smem + C::OFF_Q + t * C::TILE_BYTES;
+      if (ok && nt > 0) {
+        __syncwarp();
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + c, o);
+          tmem_wait_ld();
+          reg_fence(o);
+          const int slab = c / 64;
+          const int chunk0 = (c % 64) / 8;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 val;
+            val.x = pack_x2<BF16>(__uint_as_float(o[8 * k + 0]) * inv_l, __uint_as_float(o[8 * k + 1]) * inv_l);
+            val.y = pack_x2<BF16>(__uint_as_float(o[8 * k + 2]) * inv_l, __uint_as_float(o[8 * k + 3]) * inv_l);
+            val.z = pack_x2<BF16>(__uint_as_float(o[8 * k + 4]) * inv_l, __uint_as_float(o[8 * k + 5]) * inv_l);
+            val.w = pack_x2<BF16>(__uint_as_float(o[8 * k + 6]) * inv_l, __uint_as_float(o[8 * k + 7]) * inv_l);
+            const int phys = (chunk0 + k) ^ (r & 7);
+            *reinterpret_cast<uint4*>(stage + slab * C::SLAB_BYTES + r * 128 + phys * 16) = val;
+          }
+        }
+        fence_proxy_async_smem();
+        if (my_row < N) a.lse[static_cast<size_t>(bh) * N + my_row] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
+      }
+      // Every warp of the group reaches this barrier on every path, aborted or not.
+      named_bar_sync(1 + t, 128);
+      if ((threadIdx.x & 127) == 0 && nt > 0 && *abort_flag == 0) {
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s)
+          tma_store_3d(&tm_o, stage + s * C::SLAB_BYTES, s * 64, row_base, bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
     }
   }
   tc_fence_before();
@@ -401,7 +449,7 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   auto kern = fa2_fwd_kernel<D, BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_m_blocks, a.B, a.H);
+  dim3 grid(a.num_m_blocks * (a.num_splits > 1 ? a.num_splits : 1), a.B, a.H);
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }

@@ -73,6 +73,35 @@ typedef enum fa2_dtype { FA2_FP16 = 0, FA2_BF16 = 1 } fa2_dtype;
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
             int d, int causal, float scale, int dtype, void* stream);
 
+/* K/V-split forward ("大猿搬砖简记", thread-block section: when the (row block,
+ * batch, head) workers cannot fill the SMs, each worker's K/V range may be cut
+ * into num_splits parts run by separate blocks, whose partial results are then
+ * combined to recover the global softmax). Part s of a worker covers
+ * ceil(tiles / num_splits) of its K/V tiles of 128 keys (the last parts shorter
+ * or empty); each part writes its fp32 O / l and logsumexp into the workspace,
+ * and a merge pass forms L = ln sum_s exp(lse_s), O = sum_s exp(lse_s - L) O_s.
+ * Same result as fa2_fwd up to rounding.
+ *   num_splits : 1 .. 128 (1 runs fa2_fwd and ignores the workspace).
+ *   workspace  : device, >= fa2_fwd_split_workspace_size(...) bytes, 256-byte
+ *                aligned, scratch owned by the caller (contents ignored on
+ *                entry, undefined on exit).
+ *   other arguments as in fa2_fwd. */
+int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                  int N, int d, int causal, float scale, int dtype, int num_splits, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa2_fwd_split needs: num_splits x B*H x N x (d + 1) fp32,
+ * each of the two arrays rounded up to 256 bytes. Returns 0 for invalid sizes. */
+size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/* The split count of the same page: for each candidate s in 1 .. min(128,
+ * num_sms, ceil(N / 128)), SM utilisation = w / ceil(w) with w = workers * s /
+ * num_sms waves and workers = B * H * ceil(N / 256) forward CTAs (the page does
+ * not define utilisation; this is the filled fraction of the waves); returns
+ * the smallest s whose utilisation is at least 0.95 of the best. Host only.
+ * Returns 0 for invalid arguments. */
+int fa2_num_splits(int B, int H, int N, int d, int causal, int num_sms);
+
 /* Bytes of device workspace fa2_bwd needs: the fp32 row sums D = rowsum(dO o O)
  * and L * log2(e), each [B*H][N rounded up to 128]. Returns 0 for invalid sizes. */
 size_t fa2_bwd_workspace_size(int B, int H, int N, int d);

@@ -44,3 +44,37 @@ def test_bwd_block_work_matches_oracle(fa2_lib, N, d, causal):
         k0, k1, i0, i1 = fa2_lib.bwd_block_work(bx, N, d, causal)
         assert (k0, k1) == (bx * keys, min(N, (bx + 1) * keys))
         assert (i0, i1) == schedule.bwd_q_tile_range(bx, N, qrows, keys, causal)
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 16384), (4, 32, 8192), (2, 3, 1000),
+                                   (1, 1, 100000), (8, 16, 2048), (1, 5, 4096)])
+@pytest.mark.parametrize("num_sms", [1, 132, 148, 152, 160])
+def test_num_splits_matches_oracle(fa2_lib, B, H, N, num_sms):
+    """The library's K/V split count equals the oracle's rule (same workers:
+    one forward CTA per 256 query rows; same tiles of 128 keys)."""
+    lib = fa2_lib.load_library()
+    workers = B * H * schedule.ceil_div(N, 256)
+    want = schedule.num_splits_heuristic(workers, num_sms, schedule.ceil_div(N, 128), 128)
+    for causal in (0, 1):
+        assert lib.fa2_num_splits(B, H, N, 128, causal, num_sms) == want
+
+
+def test_num_splits_rejects_bad_arguments(fa2_lib):
+    lib = fa2_lib.load_library()
+    assert lib.fa2_num_splits(0, 1, 128, 128, 0, 152) == 0
+    assert lib.fa2_num_splits(1, 1, 128, 96, 0, 152) == 0
+    assert lib.fa2_num_splits(1, 1, 128, 128, 2, 152) == 0
+    assert lib.fa2_num_splits(1, 1, 128, 128, 0, 0) == 0
+
+
+def test_split_workspace_size(fa2_lib):
+    lib = fa2_lib.load_library()
+
+    def up(x):
+        return -(-x // 256) * 256
+
+    for B, H, N, d, S in ((1, 2, 16384, 128, 7), (2, 3, 1000, 64, 3), (1, 1, 1, 64, 1)):
+        rows = S * B * H * N
+        assert lib.fa2_fwd_split_workspace_size(B, H, N, d, S) == up(rows * d * 4) + up(rows * 4)
+    assert lib.fa2_fwd_split_workspace_size(1, 1, 128, 128, 0) == 0
+    assert lib.fa2_fwd_split_workspace_size(1, 1, 128, 128, 129) == 0
