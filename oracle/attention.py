@@ -37,7 +37,10 @@ use of the shortcut is checked against an independent route.
 Readings where the pages are silent (each listed in the design notes):
   * scale multiplies S before the mask; L is the logsumexp of the scaled S, in
     natural-log units;
-  * causal alignment is top-left with equal query and key lengths (j <= i);
+  * causal alignment is top-left (key j visible to query i iff j <= i), also
+    when the key length N_k differs from the query length N_q (the pages keep
+    seqlen_q and seqlen_k distinct but say nothing about the mask then):
+    query i sees keys 0..min(i, N_k - 1);
   * inputs arrive already rounded to the kernel dtype and are upcast to fp64.
 
 Memory: rows are processed in chunks of at most ``row_chunk`` queries; each
@@ -54,8 +57,9 @@ __all__ = ["forward", "backward", "lse_brute_force", "combine_partials"]
 
 
 def _check(q, k, v):
-    if q.ndim != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must all have shape [B, H, N, d]")
+    if (q.ndim != 4 or k.ndim != 4 or k.shape != v.shape or k.shape[:2] != q.shape[:2]
+            or k.shape[3] != q.shape[3]):
+        raise ValueError("q must be [B, H, N_q, d] and k, v [B, H, N_k, d]")
 
 
 def _scores(qc, k, row0, causal, scale):
@@ -80,12 +84,13 @@ def forward(q, k, v, causal=False, scale=None, row_chunk=1024):
     """Exact attention forward.
 
     Args:
-      q, k, v: arrays [B, H, N, d] (any float type; computed in fp64).
+      q: array [B, H, N_q, d]; k, v: arrays [B, H, N_k, d] (any float type;
+         computed in fp64). N_k may differ from N_q.
       causal: apply the top-left causal mask (key j visible to query i iff j <= i).
       scale: score scale; default 1/sqrt(d).
     Returns:
-      (o, lse): o [B, H, N, d] fp64, lse [B, H, N] fp64 natural-log logsumexp of
-      the scaled, masked scores.
+      (o, lse): o [B, H, N_q, d] fp64, lse [B, H, N_q] fp64 natural-log logsumexp
+      of the scaled, masked scores.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -111,7 +116,8 @@ def forward(q, k, v, causal=False, scale=None, row_chunk=1024):
 def backward(q, k, v, do, causal=False, scale=None, row_chunk=1024):
     """Naive chain-rule backward of ``forward`` given the output gradient dO.
 
-    Returns (dq, dk, dv), each [B, H, N, d] fp64.
+    Returns (dq, dk, dv): dq like q, dk and dv like k (fp64). A key that no
+    query sees (causal, N_k > N_q) gets zero gradients.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -119,7 +125,7 @@ def backward(q, k, v, do, causal=False, scale=None, row_chunk=1024):
     do = np.asarray(do, dtype=np.float64)
     _check(q, k, v)
     if do.shape != q.shape:
-        raise ValueError("do must have shape [B, H, N, d]")
+        raise ValueError("do must have the shape of q")
     B, H, N, d = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -148,6 +154,7 @@ def lse_brute_force(q, k, causal=False, scale=None):
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     B, H, N, d = q.shape
+    n_k = k.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     out = np.empty((B, H, N), dtype=np.float64)
@@ -155,7 +162,7 @@ def lse_brute_force(q, k, causal=False, scale=None):
         for h in range(H):
             for i in range(N):
                 vals = []
-                for j in range(N):
+                for j in range(n_k):
                     if causal and j > i:
                         continue
                     dot = 0.0

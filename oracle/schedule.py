@@ -67,16 +67,19 @@ def _tile_fully_masked(q0, q1, k0, k1):
     return k0 > q1 - 1
 
 
-def fwd_kv_tile_range(m_block: int, N: int, block_m: int, block_n: int, causal: bool):
+def fwd_kv_tile_range(m_block: int, N: int, block_m: int, block_n: int, causal: bool,
+                      n_k: int | None = None):
     """Half-open range [j_begin, j_end) of K/V tiles a forward worker visits.
+    N is the query length and n_k the key length (default N).
 
     Derived by brute force over all tiles, dropping fully masked ones, so that
     it is independent of any closed-form bound.
     """
+    n_k = N if n_k is None else n_k
     q0, q1 = m_block * block_m, min(N, (m_block + 1) * block_m)
     visited = []
-    for j in range(ceil_div(N, block_n)):
-        k0, k1 = j * block_n, min(N, (j + 1) * block_n)
+    for j in range(ceil_div(n_k, block_n)):
+        k0, k1 = j * block_n, min(n_k, (j + 1) * block_n)
         if causal and _tile_fully_masked(q0, q1, k0, k1):
             continue
         visited.append(j)
@@ -91,10 +94,14 @@ def bwd_grid(B: int, H: int, N: int, block_n: int):
     return (ceil_div(N, block_n), B, H)
 
 
-def bwd_q_tile_range(n_block: int, N: int, block_m: int, block_n: int, causal: bool):
+def bwd_q_tile_range(n_block: int, N: int, block_m: int, block_n: int, causal: bool,
+                     n_k: int | None = None):
     """Half-open range [i_begin, i_end) of Q tiles a backward column worker visits
-    (brute force over all tiles, dropping fully masked ones)."""
-    k0, k1 = n_block * block_n, min(N, (n_block + 1) * block_n)
+    (brute force over all tiles, dropping fully masked ones). N is the query
+    length and n_k the key length (default N); a worker whose keys no query
+    sees gets the empty range."""
+    n_k = N if n_k is None else n_k
+    k0, k1 = n_block * block_n, min(n_k, (n_block + 1) * block_n)
     visited = []
     for i in range(ceil_div(N, block_m)):
         q0, q1 = i * block_m, min(N, (i + 1) * block_m)

@@ -85,6 +85,28 @@ def pin_single_token(ora):
         _close(dv, do, 1e-12, "dV(N=1)")
 
 
+def pin_single_query_cross_length(ora):
+    """N_q = 1 against N_k > 1 keys. Causal (top-left): the query sees key 0
+    only, so O = V_0, L = scale q.k_0, dV_0 = dO and every other dK, dV row is
+    0. Not causal: L = ln sum_j exp(scale q.k_j), by hand."""
+    r = _rng(11)
+    q, do = (r.standard_normal((2, 2, 1, 4)) for _ in range(2))
+    k, v = (r.standard_normal((2, 2, 6, 4)) for _ in range(2))
+    o, lse = ora.forward(q, k, v, causal=True, scale=0.7)
+    dq, dk, dv = ora.backward(q, k, v, do, causal=True, scale=0.7)
+    _close(o, v[:, :, :1], 1e-12, "O(causal, N_q=1)")
+    _close(lse, 0.7 * np.sum(q[:, :, 0] * k[:, :, 0], axis=-1)[..., None], 1e-12, "L(causal, N_q=1)")
+    _close(dv[:, :, :1], do, 1e-12, "dV_0(causal, N_q=1)")
+    _close(dv[:, :, 1:], 0 * dv[:, :, 1:], 1e-12, "dV of unseen keys")
+    _close(dk, 0 * dk, 1e-12, "dK(causal, N_q=1)")
+    _close(dq, 0 * dq, 1e-12, "dQ(causal, N_q=1)")
+    _, lse = ora.forward(q, k, v, causal=False, scale=0.7)
+    for b in range(2):
+        for h in range(2):
+            want = math.log(sum(math.exp(0.7 * float(np.dot(q[b, h, 0], k[b, h, j]))) for j in range(6)))
+            _close(lse[b, h, 0], want, 1e-12, "L(N_q=1)")
+
+
 def pin_constant_values(ora):
     """All V rows equal c: O_i = c whatever P is, and the output no longer
     depends on Q or K, so dQ = dK = 0."""
@@ -133,10 +155,12 @@ def pin_two_tokens_by_hand(ora):
 # Brute force
 # ---------------------------------------------------------------------------
 def pin_lse_brute_force(ora):
-    """L equals the row logsumexp computed by pure-Python loops."""
+    """L equals the row logsumexp computed by pure-Python loops, for equal and
+    for different query and key lengths."""
     r = _rng(5)
-    for (B, H, N, d) in ((1, 1, 5, 3), (2, 2, 7, 4)):
-        q, k, v = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    for (B, H, N, Nk, d) in ((1, 1, 5, 5, 3), (2, 2, 7, 7, 4), (1, 2, 4, 9, 3), (2, 1, 9, 4, 3)):
+        q = r.standard_normal((B, H, N, d))
+        k, v = (r.standard_normal((B, H, Nk, d)) for _ in range(2))
         for causal in (False, True):
             _, lse = ora.forward(q, k, v, causal=causal, scale=0.45, row_chunk=3)
             _close(lse, ora.lse_brute_force(q, k, causal=causal, scale=0.45), 1e-12, "L brute")
@@ -280,24 +304,29 @@ def pin_sdpa_cross_check(ora):
     import torch.nn.functional as F
 
     r = _rng(10)
-    B, H, N, d = 2, 3, 17, 8
-    q, k, v, do = (r.standard_normal((B, H, N, d)) for _ in range(4))
-    for causal in (False, True):
-        tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
-        out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.3)
-        out.backward(torch.tensor(do, dtype=torch.float64))
-        o, _ = ora.forward(q, k, v, causal=causal, scale=0.3)
-        dq, dk, dv = ora.backward(q, k, v, do, causal=causal, scale=0.3)
-        _close(o, out.detach().numpy(), 1e-12, "SDPA O")
-        _close(dq, tq.grad.numpy(), 1e-12, "SDPA dQ")
-        _close(dk, tk.grad.numpy(), 1e-12, "SDPA dK")
-        _close(dv, tv.grad.numpy(), 1e-12, "SDPA dV")
+    B, H, d = 2, 3, 8
+    # Equal lengths, and both orders of different query / key lengths (torch's
+    # is_causal mask is top-left aligned for a non-square score matrix).
+    for N, Nk in ((17, 17), (5, 13), (13, 5)):
+        q, do = (r.standard_normal((B, H, N, d)) for _ in range(2))
+        k, v = (r.standard_normal((B, H, Nk, d)) for _ in range(2))
+        for causal in (False, True):
+            tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+            out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=causal, scale=0.3)
+            out.backward(torch.tensor(do, dtype=torch.float64))
+            o, _ = ora.forward(q, k, v, causal=causal, scale=0.3)
+            dq, dk, dv = ora.backward(q, k, v, do, causal=causal, scale=0.3)
+            _close(o, out.detach().numpy(), 1e-12, "SDPA O")
+            _close(dq, tq.grad.numpy(), 1e-12, "SDPA dQ")
+            _close(dk, tk.grad.numpy(), 1e-12, "SDPA dK")
+            _close(dv, tv.grad.numpy(), 1e-12, "SDPA dV")
 
 
 ALL_PINS = [
     pin_zero_query,
     pin_causal_row_zero,
     pin_single_token,
+    pin_single_query_cross_length,
     pin_constant_values,
     pin_two_tokens_by_hand,
     pin_lse_brute_force,

@@ -109,3 +109,25 @@ def test_split_kv_range_partitions_the_range(j0, j1):
         per = schedule.ceil_div(j1 - j0, S) if j1 > j0 else 0
         assert all(hi - lo <= per for lo, hi in parts)
         assert all(j0 <= lo <= hi <= j1 for lo, hi in parts)
+
+
+@pytest.mark.parametrize("N,Nk", [(1, 300), (300, 1), (130, 500), (500, 130), (256, 257)])
+def test_cross_length_tile_ranges_match_element_level_brute_force(N, Nk):
+    """Query length N, key length Nk: a tile pair is visited iff some (query,
+    key) element in it is visible (top-left causal: key <= query)."""
+    bm = bn = 128
+    for causal in (False, True):
+        for m in range(schedule.ceil_div(N, bm)):
+            j0, j1 = schedule.fwd_kv_tile_range(m, N, bm, bn, causal, n_k=Nk)
+            for j in range(schedule.ceil_div(Nk, bn)):
+                visible = any((not causal) or kk <= qq
+                              for qq in range(m * bm, min(N, (m + 1) * bm))
+                              for kk in range(j * bn, min(Nk, (j + 1) * bn)))
+                assert (j0 <= j < j1) == visible, (m, j, causal)
+        for n in range(schedule.ceil_div(Nk, bn)):
+            i0, i1 = schedule.bwd_q_tile_range(n, N, bm, bn, causal, n_k=Nk)
+            for i in range(schedule.ceil_div(N, bm)):
+                visible = any((not causal) or kk <= qq
+                              for qq in range(i * bm, min(N, (i + 1) * bm))
+                              for kk in range(n * bn, min(Nk, (n + 1) * bn)))
+                assert (i0 <= i < i1) == visible, (n, i, causal)
