@@ -68,6 +68,8 @@ def load_library() -> ctypes.CDLL:
         "fa2_fwd": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]),
         "fa2_fwd_instrumented": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp]),
         "fa2_fwd_split": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz, vp]),
+        "fa2_fwd_qk": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]),
+        "fa2_bwd_qk": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]),
         "fa2_fwd_split_workspace_size": (sz, [i, i, i, i, i]),
         "fa2_num_splits": (i, [i, i, i, i, i, i]),
         "fa2_bwd_workspace_size": (sz, [i, i, i, i]),
@@ -134,16 +136,19 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
 
     ``num_splits`` > 1 cuts each worker's K/V range into that many parts run by
     separate CTAs and merges them (fa2_fwd_split); "auto" picks the count with
-    the library's rule for this GPU. Returns (o, lse): o like q, lse float32
-    [B, H, N] (natural log).
+    the library's rule for this GPU. k and v may have their own length N_k
+    (fa2_fwd_qk; causal mask top-left: query i sees keys 0..i). Returns
+    (o, lse): o like q, lse float32 [B, H, N] (natural log).
     """
     B, H, N, d = _shape(q)
+    Nk = _shape(k)[2]
     dt = q.dtype
     if dt not in _DTYPES:
         raise ValueError("q must be float16 or bfloat16")
     dev = q.device
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_tensor(name, t, (B, H, N, d), dt, dev)
+    _check_tensor("q", q, (B, H, N, d), dt, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check_tensor(name, t, (B, H, Nk, d), dt, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -153,6 +158,14 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     _check_tensor("out", out, (B, H, N, d), dt, dev)
     _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
     lib = load_library()
+    if Nk != N:
+        if num_splits not in (1, "auto"):
+            raise ValueError("a K/V split needs equal query and key lengths")
+        code = lib.fa2_fwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, N, Nk, d, int(bool(causal)), float(scale),
+                              _DTYPES[dt], _stream_ptr(dev))
+        _check("fa2_fwd_qk", code)
+        return out, lse
     if num_splits == "auto":
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         num_splits = int(lib.fa2_num_splits(B, H, N, d, int(bool(causal)), sms))
@@ -198,26 +211,39 @@ def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
              dq=None, dk=None, dv=None, workspace=None):
-    """Gradients (dq, dk, dv) of the attention output given dO."""
+    """Gradients (dq, dk, dv) of the attention output given dO. k and v may
+    have their own length N_k (fa2_bwd_qk)."""
     B, H, N, d = _shape(q)
+    Nk = _shape(k)[2]
     dt = q.dtype
     if dt not in _DTYPES:
         raise ValueError("q must be float16 or bfloat16")
     dev = q.device
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+    for name, t in (("q", q), ("o", o), ("do", do)):
         _check_tensor(name, t, (B, H, N, d), dt, dev)
+    for name, t in (("k", k), ("v", v)):
+        _check_tensor(name, t, (B, H, Nk, d), dt, dev)
     _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_tensor(name, t, (B, H, N, d), dt, dev)
+    _check_tensor("dq", dq, (B, H, N, d), dt, dev)
+    for name, t in (("dk", dk), ("dv", dv)):
+        _check_tensor(name, t, (B, H, Nk, d), dt, dev)
     need = bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     lib = load_library()
+    if Nk != N:
+        code = lib.fa2_bwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, Nk, d, int(bool(causal)), float(scale),
+                              _DTYPES[dt], workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), _stream_ptr(dev))
+        _check("fa2_bwd_qk", code)
+        return dq, dk, dv
     code = lib.fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                        do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
                        int(bool(causal)), float(scale), _DTYPES[dt], workspace.data_ptr(),

@@ -137,19 +137,25 @@ int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dt
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// N: query length (q, o, lse); Nk: key length (k, v).
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-             int d, int causal, float scale, int dtype, int* tile_counts, void* stream,
+             int Nk, int d, int causal, float scale, int dtype, int* tile_counts, void* stream,
              int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0) {
   if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
   int st = check_common(B, H, N, d, causal, scale, dtype);
   if (st != FA2_OK) return st;
+  st = check_common(B, H, Nk, d, causal, scale, dtype);
+  if (st != FA2_OK) return st;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return FA2_ERR_ALIGNMENT;
-  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;   // q, o
+  const size_t kbytes = static_cast<size_t>(B) * H * Nk * d * 2;  // k, v
   const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
   const void* ins[3] = {q, k, v};
-  for (const void* in : ins)
-    if (overlap(o, tbytes, in, tbytes) || overlap(lse, lbytes, in, tbytes)) return FA2_ERR_OVERLAP;
+  const size_t in_bytes[3] = {tbytes, kbytes, kbytes};
+  for (int x = 0; x < 3; ++x)
+    if (overlap(o, tbytes, ins[x], in_bytes[x]) || overlap(lse, lbytes, ins[x], in_bytes[x]))
+      return FA2_ERR_OVERLAP;
   if (overlap(o, tbytes, lse, lbytes)) return FA2_ERR_OVERLAP;
   const int BH = B * H;
   float* o_part = nullptr;
@@ -158,8 +164,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     const size_t need = fa2_fwd_split_workspace_size(B, H, N, d, num_splits);
     if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return FA2_ERR_ALIGNMENT;
-    for (const void* in : ins)
-      if (overlap(workspace, need, in, tbytes)) return FA2_ERR_OVERLAP;
+    for (int x = 0; x < 3; ++x)
+      if (overlap(workspace, need, ins[x], in_bytes[x])) return FA2_ERR_OVERLAP;
     if (overlap(workspace, need, o, tbytes) || overlap(workspace, need, lse, lbytes))
       return FA2_ERR_OVERLAP;
     o_part = static_cast<float*>(workspace);
@@ -171,14 +177,15 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   st = device_setup(&dev, &status);
   if (st != FA2_OK) return st;
   CUtensorMap tq, tk, tv, to;
-  if (make_map_16bit(&tq, q, BH, N, d, dtype) || make_map_16bit(&tk, k, BH, N, d, dtype) ||
-      make_map_16bit(&tv, v, BH, N, d, dtype) || make_map_16bit(&to, o, BH, N, d, dtype))
+  if (make_map_16bit(&tq, q, BH, N, d, dtype) || make_map_16bit(&tk, k, BH, Nk, d, dtype) ||
+      make_map_16bit(&tv, v, BH, Nk, d, dtype) || make_map_16bit(&to, o, BH, N, d, dtype))
     return FA2_ERR_CUDA;
   fa2::FwdArgs a{};
   a.lse = lse;
   a.B = B;
   a.H = H;
   a.N = N;
+  a.Nk = Nk;
   a.num_m_blocks = fa2::fwd_num_m_blocks(N);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
@@ -216,7 +223,12 @@ extern "C" {
 
 int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
             int d, int causal, float scale, int dtype, void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, nullptr, stream);
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, causal, scale, dtype, nullptr, stream);
+}
+
+int fa2_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Nq, int Nk, int d, int causal, float scale, int dtype, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, dtype, nullptr, stream);
 }
 
 size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits) {
@@ -240,14 +252,14 @@ int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* l
                   int N, int d, int causal, float scale, int dtype, int num_splits, void* workspace,
                   size_t workspace_bytes, void* stream) {
   if (num_splits < 1 || num_splits > kMaxFwdSplits) return FA2_ERR_INVALID_ARG;
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, nullptr, stream, num_splits,
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, causal, scale, dtype, nullptr, stream, num_splits,
                   workspace, workspace_bytes);
 }
 
 int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int N, int d, int causal, float scale, int dtype, int* tile_counts,
                          void* stream) {
-  return fwd_impl(q, k, v, o, lse, B, H, N, d, causal, scale, dtype, tile_counts, stream);
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, causal, scale, dtype, tile_counts, stream);
 }
 
 size_t fa2_bwd_workspace_size(int B, int H, int N, int d) {
@@ -259,12 +271,16 @@ size_t fa2_bwd_workspace_size(int B, int H, int N, int d) {
   return 2 * align_up(bh * n_pad * 4, 256);
 }
 
-int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, const float* lse,
-                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
-                  int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
-                  void* const* phase_events, void* stream) {
+namespace {
+// N: query length (q, o, dO, dq, lse); Nk: key length (k, v, dk, dv).
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int Nk, int d,
+             int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+             void* const* phase_events, void* stream) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
   int st = check_common(B, H, N, d, causal, scale, dtype);
+  if (st != FA2_OK) return st;
+  st = check_common(B, H, Nk, d, causal, scale, dtype);
   if (st != FA2_OK) return st;
   const void* in16[5] = {q, k, v, o, dO};
   void* out16[3] = {dq, dk, dv};
@@ -276,19 +292,21 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
   const size_t need = fa2_bwd_workspace_size(B, H, N, d);
   if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA2_ERR_ALIGNMENT;
-  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t qb = static_cast<size_t>(B) * H * N * d * 2;   // q, o, dO, dq
+  const size_t kb = static_cast<size_t>(B) * H * Nk * d * 2;  // k, v, dk, dv
   const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
-  for (void* out : out16) {
-    for (const void* in : in16)
-      if (overlap(out, tbytes, in, tbytes)) return FA2_ERR_OVERLAP;
-    if (overlap(out, tbytes, lse, lbytes) || overlap(out, tbytes, workspace, need))
+  const size_t in_b[5] = {qb, kb, kb, qb, qb};
+  const size_t out_b[3] = {qb, kb, kb};
+  for (int x = 0; x < 3; ++x) {
+    for (int y = 0; y < 5; ++y)
+      if (overlap(out16[x], out_b[x], in16[y], in_b[y])) return FA2_ERR_OVERLAP;
+    if (overlap(out16[x], out_b[x], lse, lbytes) || overlap(out16[x], out_b[x], workspace, need))
       return FA2_ERR_OVERLAP;
   }
-  if (overlap(dq, tbytes, dk, tbytes) || overlap(dq, tbytes, dv, tbytes) ||
-      overlap(dk, tbytes, dv, tbytes))
+  if (overlap(dq, qb, dk, kb) || overlap(dq, qb, dv, kb) || overlap(dk, kb, dv, kb))
     return FA2_ERR_OVERLAP;
-  for (const void* in : in16)
-    if (overlap(workspace, need, in, tbytes)) return FA2_ERR_OVERLAP;
+  for (int y = 0; y < 5; ++y)
+    if (overlap(workspace, need, in16[y], in_b[y])) return FA2_ERR_OVERLAP;
   if (overlap(workspace, need, lse, lbytes)) return FA2_ERR_OVERLAP;
   int dev = 0;
   int* status = nullptr;
@@ -298,8 +316,9 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
   // Tensor maps: q, k, v, dO (loads), dk, dv, dq (stores); all 128-row boxes.
   CUtensorMap maps[7];
   const void* src[7] = {q, k, v, dO, dk, dv, dq};
+  const int rows[7] = {N, Nk, Nk, N, Nk, Nk, N};
   for (int i = 0; i < 7; ++i)
-    if (make_map_16bit(&maps[i], src[i], BH, N, d, dtype) != FA2_OK) return FA2_ERR_CUDA;
+    if (make_map_16bit(&maps[i], src[i], BH, rows[i], d, dtype) != FA2_OK) return FA2_ERR_CUDA;
   const size_t n_pad = align_up(static_cast<size_t>(N), 128);
   const size_t lbytes_pad = align_up(static_cast<size_t>(BH) * n_pad * 4, 256);
   float* dsum = static_cast<float*>(workspace);
@@ -311,6 +330,7 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
   a.B = B;
   a.H = H;
   a.N = N;
+  a.Nk = Nk;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
@@ -321,6 +341,23 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
       static_cast<cudaStream_t>(stream),
       reinterpret_cast<cudaEvent_t*>(const_cast<void**>(phase_events)));
   return e == cudaSuccess ? FA2_OK : cuda_fail(e);
+}
+}  // namespace
+
+int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                  int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                  void* const* phase_events, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, causal, scale, dtype, workspace,
+                  workspace_bytes, phase_events, stream);
+}
+
+int fa2_bwd_qk(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dO, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+               int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, causal, scale, dtype,
+                  workspace, workspace_bytes, nullptr, stream);
 }
 
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -215,7 +215,7 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uin
 // would otherwise keep the exponentials from overlapping.
 template <bool MASK, bool CAUSAL>
 __device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const float* nl_cols, float sl2,
-                                            int kg, int q_first, int N, float* p) {
+                                            int kg, int q_first, int Nq, int Nk, float* p) {
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     const float2 x = f2_fma(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
@@ -223,8 +223,8 @@ __device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const floa
     float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
     if constexpr (MASK) {
       const int q0 = q_first + c;
-      p0 = (kg >= N || q0 >= N || (CAUSAL && kg > q0)) ? 0.f : p0;
-      p1 = (kg >= N || q0 + 1 >= N || (CAUSAL && kg > q0 + 1)) ? 0.f : p1;
+      p0 = (kg >= Nk || q0 >= Nq || (CAUSAL && kg > q0)) ? 0.f : p0;
+      p1 = (kg >= Nk || q0 + 1 >= Nq || (CAUSAL && kg > q0 + 1)) ? 0.f : p1;
     }
     p[c] = p0;
     p[c + 1] = p1;
@@ -302,12 +302,15 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ BwdKvShared sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.N;
+  const int N = a.N;    // queries
+  const int Nk = a.Nk;  // keys and values
   const int nb = blockIdx.x;                     // key block, fastest grid axis
   const int bh = blockIdx.y * a.H + blockIdx.z;  // grid = (n block, batch, head)
   const int n0 = nb * kTileRows;
   const int i_begin = bwd_q_tile_begin(nb, CAUSAL);
-  const int n_steps = ceil_div(N, kTileRows) - i_begin;
+  // 0 when no query sees these keys (causal, more keys than queries): the
+  // block then loads and issues nothing and writes dK = dV = 0.
+  const int n_steps = max(0, ceil_div(N, kTileRows) - i_begin);
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
@@ -343,9 +346,11 @@ __global__ void __launch_bounds__(384, 1)
       // ---------------- TMA producer ----------------
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
-      load_tile<D>(smem + C::OFF_FIX0, &tm_k, &sh.kv_full, n0, bh);
-      load_tile<D>(smem + C::OFF_FIX1, &tm_v, &sh.kv_full, n0, bh);
+      if (n_steps > 0) {
+        mbar_arrive_expect_tx(&sh.kv_full, 2 * C::TILE_BYTES);
+        load_tile<D>(smem + C::OFF_FIX0, &tm_k, &sh.kv_full, n0, bh);
+        load_tile<D>(smem + C::OFF_FIX1, &tm_v, &sh.kv_full, n0, bh);
+      }
       int i = 0;
       bool ok = true;
       for (; i < n_steps; ++i) {
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__(384, 1)
         load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_do, &sh.do_full[st], q0, bh);
       }
       if (!ok) {
-        mbar_wait_drain(&sh.kv_full, 0, a.timeout_ns);
+        if (n_steps > 0) mbar_wait_drain(&sh.kv_full, 0, a.timeout_ns);
         for (int ii = max(0, i - C::NS); ii < i; ++ii) {
           mbar_wait_drain(&sh.q_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
           mbar_wait_drain(&sh.do_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
@@ -374,8 +379,9 @@ __global__ void __launch_bounds__(384, 1)
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
       auto q_at = [&](int i) { return smem_u32(smem + C::OFF_STR0 + (i % C::NS) * C::TILE_BYTES); };
       auto do_at = [&](int i) { return smem_u32(smem + C::OFF_STR1 + (i % C::NS) * C::TILE_BYTES); };
-      bool ok = mbar_wait_warp(&sh.kv_full, 0, wc) && mbar_wait_warp(&sh.q_full[0], 0, wc);
-      if (ok) {
+      bool ok = n_steps == 0 ||
+                (mbar_wait_warp(&sh.kv_full, 0, wc) && mbar_wait_warp(&sh.q_full[0], 0, wc));
+      if (ok && n_steps > 0) {
         tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(0));
         umma_commit_warp(&sh.st_full);
@@ -487,7 +493,7 @@ __global__ void __launch_bounds__(384, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.st_free);
       const bool need_mask = (CAUSAL && qc0 < n0 + kTileRows - 1) || (qc0 + 64 > N) ||
-                             (n0 + kTileRows > N);
+                             (n0 + kTileRows > Nk);
       // P^T as 16-bit pairs; dS^T below is formed from these rounded values.
       uint32_t pk[32];
 #pragma unroll
@@ -495,9 +501,9 @@ __global__ void __launch_bounds__(384, 1)
         float p[32];
         const uint32_t(&sh_h)[32] = *reinterpret_cast<const uint32_t(*)[32]>(&sv[32 * h]);
         if (need_mask)
-          dkdv_p_cols<true, CAUSAL>(sh_h, lreg + 32 * h, sl2, kg, qc0 + 32 * h, N, p);
+          dkdv_p_cols<true, CAUSAL>(sh_h, lreg + 32 * h, sl2, kg, qc0 + 32 * h, N, Nk, p);
         else
-          dkdv_p_cols<false, CAUSAL>(sh_h, lreg + 32 * h, sl2, kg, qc0 + 32 * h, N, p);
+          dkdv_p_cols<false, CAUSAL>(sh_h, lreg + 32 * h, sl2, kg, qc0 + 32 * h, N, Nk, p);
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[16 * h + j] = pack_x2<BF16>(p[2 * j], p[2 * j + 1]);
       }
@@ -541,11 +547,19 @@ __global__ void __launch_bounds__(384, 1)
     if (ok) ok = mbar_wait_warp(&sh.mma_done, 0, wc);
     // All MMAs have completed, so the K and V buffers are free for staging.
     uint8_t* stage = smem + (wg == 0 ? C::OFF_FIX1 : C::OFF_FIX0);
-    if (ok) {
+    if (ok && n_steps > 0) {
       __syncwarp();
       tc_fence_after();
       stage_rows<D, BF16>(stage, tmem + lane_off + (wg == 0 ? C::KV_DV : C::KV_DK), r,
                           wg == 0 ? 1.f : a.scale);
+      fence_proxy_async_smem();
+    } else if (ok) {
+      // No query sees these keys: their gradients are zero.
+#pragma unroll
+      for (int sl = 0; sl < D / 64; ++sl)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(stage + sl * C::SLAB_BYTES + r * 128 + c * 16) = make_uint4(0u, 0u, 0u, 0u);
       fence_proxy_async_smem();
     }
     named_bar_sync(1 + wg, 128);
@@ -586,7 +600,7 @@ __global__ void __launch_bounds__(384, 1)
   const int mb = dq_m_block_of(blockIdx.x, num_m_blocks, CAUSAL);
   const int bh = blockIdx.y * a.H + blockIdx.z;
   const int q0 = mb * kTileRows;
-  const int n_kv = fwd_kv_tile_end(q0, min(N, q0 + kTileRows), N, CAUSAL);
+  const int n_kv = fwd_kv_tile_end(q0, min(N, q0 + kTileRows), a.Nk, CAUSAL);
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
@@ -713,8 +727,8 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.s_free);
-      const bool need_mask = (CAUSAL && kc0 + 63 > q0) || (kc0 + 64 > N) || (q0 + kTileRows > N);
-      const int lim = CAUSAL ? min(N, my_row + 1) : N;  // keys < lim are visible
+      const bool need_mask = (CAUSAL && kc0 + 63 > q0) || (kc0 + 64 > a.Nk) || (q0 + kTileRows > N);
+      const int lim = CAUSAL ? min(a.Nk, my_row + 1) : a.Nk;  // keys < lim are visible
       const bool row_ok = my_row < N;
       uint32_t dsp[32];
       if (need_mask)
@@ -788,7 +802,7 @@ static cudaError_t launch_bwd_t(const void* o, const void* dO, const float* lse,
     auto kern = fa2_bwd_dkdv_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
-    dim3 grid(bwd_num_n_blocks(a.N), a.B, a.H);
+    dim3 grid(bwd_num_n_blocks(a.Nk), a.B, a.H);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
                                                       maps[5], a);
     e = cudaGetLastError();

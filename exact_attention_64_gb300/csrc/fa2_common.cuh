@@ -32,9 +32,12 @@ __host__ __device__ inline int fwd_m_block_of(int block_x, int num_m_blocks, int
 // Under the causal mask a K/V tile whose first key is past the last query row
 // is entirely masked and is skipped, neither loaded nor computed
 // ("flash-attention123和ring-attention", 优化3).
-__host__ __device__ inline int fwd_kv_tile_end(int row_begin, int row_end, int N, int causal) {
+// N_k is the key length; with causal masking (top-left: key j visible to
+// query i iff j <= i) the range also stops at the last tile of the keys.
+__host__ __device__ inline int fwd_kv_tile_end(int row_begin, int row_end, int N_k, int causal) {
   if (row_end <= row_begin) return 0;
-  return causal ? ceil_div(row_end, kTileRows) : ceil_div(N, kTileRows);
+  const int all = ceil_div(N_k, kTileRows);
+  return causal ? min(ceil_div(row_end, kTileRows), all) : all;
 }
 
 // KV split ("大猿搬砖简记", thread-block section, the num_splits_heuristic_fwd
@@ -93,7 +96,8 @@ __host__ __device__ inline int dq_m_block_of(int block_x, int num_m_blocks, int 
 // __grid_constant__ parameters).
 struct FwdArgs {
   float* lse;         // [B*H, N] fp32, natural-log logsumexp
-  int B, H, N;
+  int B, H, N;        // N: query length
+  int Nk;             // key (and value) length
   int num_m_blocks;   // ceil(N / 256)
   float scale_log2;   // scale * log2(e)
   int* status;        // device status word
@@ -109,7 +113,8 @@ struct BwdArgs {
   const float* l2_pad;    // L * log2(e), [B*H, n_pad] fp32 (0 past row N)
   const float* dsum_pad;  // D = rowsum(dO o O), [B*H, n_pad] fp32 (0 past row N)
   int n_pad;              // N rounded up to 128
-  int B, H, N;
+  int B, H, N;            // N: query length
+  int Nk;                 // key (and value) length
   float scale;            // softmax scale
   float scale_log2;       // scale * log2(e)
   int* status;

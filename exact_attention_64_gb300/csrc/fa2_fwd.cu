@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(384, 1)
   __shared__ FwdShared<D> sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int N = a.N;
+  const int N = a.N;    // queries
+  const int Nk = a.Nk;  // keys and values
   // grid = (m block x K/V part, batch, head); without a split there is one part.
   const int S = a.num_splits > 1 ? a.num_splits : 1;
   const int split = blockIdx.x % S;
@@ -121,8 +122,8 @@ __global__ void __launch_bounds__(384, 1)
   const int row0 = mb * kFwdRowsPerCta;
   const int rows_a = min(kTileRows, N - row0);
   const int rows_b = max(0, min(kTileRows, N - row0 - kTileRows));
-  const int end_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, N, CAUSAL),
-                        fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, N, CAUSAL)};
+  const int end_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, Nk, CAUSAL),
+                        fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, Nk, CAUSAL)};
   // This CTA's part [kv_lo, kv_hi) of the K/V tiles. Below, j counts tiles
   // within the part (ring slots, phases, first-tile flags); kv_lo + j is the
   // K/V tile itself (TMA coordinates, masks).
@@ -286,9 +287,9 @@ __global__ void __launch_bounds__(384, 1)
       reg_fence(s);
       // Mask keys past the sequence end and, on the diagonal tile, keys after the query.
       const int kv0 = (kv_lo + j) * kTileRows;
-      const bool need_mask = (kv0 + kTileRows > N) || (CAUSAL && kv0 + kTileRows - 1 > row_base);
+      const bool need_mask = (kv0 + kTileRows > Nk) || (CAUSAL && kv0 + kTileRows - 1 > row_base);
       if (need_mask) {
-        const int lim = CAUSAL ? min(N - kv0, my_row - kv0 + 1) : (N - kv0);
+        const int lim = CAUSAL ? min(Nk - kv0, my_row - kv0 + 1) : (Nk - kv0);
 #pragma unroll
         for (int c = 0; c < 128; ++c)
           if (c >= lim) s[c] = __float_as_uint(-INFINITY);

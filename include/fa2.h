@@ -18,7 +18,8 @@
  *
  * Layout of every tensor argument: contiguous row-major [B][H][N][d] of 16-bit
  * floats (dtype FA2_FP16 or FA2_BF16); lse is contiguous fp32 [B][H][N].
- * Q, K and V share the sequence length N (self-attention).
+ * Q, K and V share the sequence length N (self-attention), except in
+ * fa2_fwd_qk / fa2_bwd_qk, where K and V have their own length Nk.
  *
  * Ownership: the caller allocates and owns every buffer, including the
  * backward workspace. The library keeps only a per-device status word (a
@@ -102,6 +103,15 @@ size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits);
  * Returns 0 for invalid arguments. */
 int fa2_num_splits(int B, int H, int N, int d, int causal, int num_sms);
 
+/* Forward with different query and key lengths: q, o [B][H][Nq][d], lse
+ * [B][H][Nq]; k, v [B][H][Nk][d]. The pages keep seqlen_q and seqlen_k
+ * distinct ("FlashAttention学习笔记(2)", V2中的thread blocks排布) without stating
+ * the causal mask for unequal lengths; here it is top-left: key j is visible
+ * to query i iff j <= i, so query i sees keys 0 .. min(i, Nk - 1). Keys past
+ * Nk are masked. Other arguments and limits as in fa2_fwd (for Nq and Nk). */
+int fa2_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Nq, int Nk, int d, int causal, float scale, int dtype, void* stream);
+
 /* Bytes of device workspace fa2_bwd needs: the fp32 row sums D = rowsum(dO o O)
  * and L * log2(e), each [B*H][N rounded up to 128]. Returns 0 for invalid sizes. */
 size_t fa2_bwd_workspace_size(int B, int H, int N, int d);
@@ -120,6 +130,15 @@ size_t fa2_bwd_workspace_size(int B, int H, int N, int d);
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
             const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
             float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward with different query and key lengths (mask as in fa2_fwd_qk): q, o,
+ * dO, dq [B][H][Nq][d], lse [B][H][Nq]; k, v, dk, dv [B][H][Nk][d]. Keys that
+ * no query sees (causal, Nk > Nq) get dk = dv = 0. The workspace is
+ * fa2_bwd_workspace_size(B, H, Nq, d) bytes. Other arguments as in fa2_bwd. */
+int fa2_bwd_qk(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dO, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+               int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+               void* stream);
 
 /* fa2_bwd, plus: phase_events (4 cudaEvent_t created by the caller, or NULL)
  * are recorded on `stream` before the preprocessing kernel, between it and
