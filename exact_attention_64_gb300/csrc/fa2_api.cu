@@ -1,6 +1,7 @@
 // C ABI of libfa2.so: argument validation, TMA tensor maps, the device status
 // word and the kernel launches. Declarations and argument contracts live in
 // include/fa2.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -15,8 +16,6 @@ namespace fa2 {
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
                        cudaStream_t stream);
-cudaError_t launch_fwd_combine(int d, bool bf16, const float* o_part, const float* lse_part, void* o,
-                               float* lse, int S, long long rows, int num_sms, cudaStream_t stream);
 cudaError_t launch_bwd(int d, bool bf16, bool causal, const void* o, const void* dO,
                        const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
                        float* l2, cudaStream_t stream, cudaEvent_t* ev);
@@ -160,6 +159,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   const int BH = B * H;
   float* o_part = nullptr;
   float* lse_part = nullptr;
+  int* part_done = nullptr;
+  size_t part_done_bytes = 0;
   if (num_splits > 1) {
     const size_t need = fa2_fwd_split_workspace_size(B, H, N, d, num_splits);
     if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
@@ -169,8 +170,11 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if (overlap(workspace, need, o, tbytes) || overlap(workspace, need, lse, lbytes))
       return FA2_ERR_OVERLAP;
     o_part = static_cast<float*>(workspace);
-    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                        align_up(static_cast<size_t>(num_splits) * BH * N * d * 4, 256));
+    const size_t rows = static_cast<size_t>(num_splits) * BH * N;
+    lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(rows * d * 4, 256));
+    part_done = reinterpret_cast<int*>(static_cast<char*>(workspace) + align_up(rows * d * 4, 256) +
+                                       align_up(rows * 4, 256));
+    part_done_bytes = static_cast<size_t>(BH) * fa2::fwd_num_m_blocks(N) * 2 * sizeof(int);
   }
   int dev = 0;
   int* status = nullptr;
@@ -193,8 +197,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
   a.fault = 0;
   a.num_splits = num_splits;
+  a.kv_tiles_max = 0;
+  for (int m = 0; m < a.num_m_blocks; ++m)
+    a.kv_tiles_max = std::max(a.kv_tiles_max, fa2::fwd_block_tiles(m, N, Nk, causal));
+  a.o = o;
   a.o_part = o_part;
   a.lse_part = lse_part;
+  a.part_done = part_done;
   if (num_splits <= 1) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_fault_kind != 0) {
@@ -206,14 +215,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   // A non-sticky error left in this thread by another caller would otherwise be
   // reported as ours by the post-launch check.
   (void)cudaGetLastError();
-  cudaError_t e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
-                                  static_cast<cudaStream_t>(stream));
-  if (e == cudaSuccess && num_splits > 1) {
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    e = fa2::launch_fwd_combine(d, dtype == FA2_BF16, o_part, lse_part, o, lse, num_splits,
-                                static_cast<long long>(BH) * N, sms, static_cast<cudaStream_t>(stream));
-  }
+  cudaError_t e = cudaSuccess;
+  // The split kernel's arrival counters start at zero on every call.
+  if (part_done != nullptr)
+    e = cudaMemsetAsync(part_done, 0, part_done_bytes, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess)
+    e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
+                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA2_OK : cuda_fail(e);
 }
 
@@ -236,8 +244,10 @@ size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits) 
       num_splits > kMaxFwdSplits)
     return 0;
   // [O parts: num_splits x B*H x N x d fp32][lse parts: num_splits x B*H x N fp32]
+  // [arrival counters: B*H x ceil(N / 256) x 2 int32]
   const size_t rows = static_cast<size_t>(num_splits) * B * H * N;
-  return align_up(rows * d * 4, 256) + align_up(rows * 4, 256);
+  const size_t counters = static_cast<size_t>(B) * H * fa2::fwd_num_m_blocks(N) * 2 * sizeof(int);
+  return align_up(rows * d * 4, 256) + align_up(rows * 4, 256) + align_up(counters, 256);
 }
 
 int fa2_num_splits(int B, int H, int N, int d, int causal, int num_sms) {

@@ -42,13 +42,38 @@ __host__ __device__ inline int fwd_kv_tile_end(int row_begin, int row_end, int N
 
 // KV split ("大猿搬砖简记", thread-block section, the num_splits_heuristic_fwd
 // paragraph). When the (row block, batch, head) workers cannot fill the SMs,
-// each worker's K/V tile range [0, end) is cut into num_splits contiguous parts
-// of ceil(end / num_splits) tiles (the last parts shorter or empty); part s is
-// [lo, hi). The partial results are merged by the online-softmax rule.
-__host__ __device__ inline void fwd_split_range(int end, int num_splits, int split, int* lo, int* hi) {
-  const int per = end > 0 ? ceil_div(end, num_splits) : 0;
-  *lo = min(split * per, end);
-  *hi = min(*lo + per, end);
+// the K/V tile range [0, n) of a worker is cut into contiguous parts merged
+// later by the online-softmax rule. num_splits is the part count of the
+// longest range (n_max tiles); a shorter range (causal row blocks) gets
+// proportionally fewer parts, min(n, ceil(n * num_splits / n_max)), so that no
+// part is empty and none is longer than ceil(n_max / num_splits) tiles.
+__host__ __device__ inline int fwd_num_parts(int n, int num_splits, int n_max) {
+  if (n <= 0) return 0;
+  if (num_splits <= 1 || n_max <= 0) return 1;
+  const long long p = (static_cast<long long>(n) * num_splits + n_max - 1) / n_max;
+  return static_cast<int>(p < n ? p : n);
+}
+
+// Part `part` of `parts` balanced parts of [0, n): [floor(part n / parts),
+// floor((part + 1) n / parts)); every part is non-empty when parts <= n.
+__host__ __device__ inline void fwd_part_range(int n, int parts, int part, int* lo, int* hi) {
+  if (parts <= 0) { *lo = *hi = 0; return; }
+  *lo = static_cast<int>(static_cast<long long>(part) * n / parts);
+  *hi = static_cast<int>(static_cast<long long>(part + 1) * n / parts);
+}
+
+// K/V tile count of row block m (kFwdRowsPerCta query rows).
+__host__ __device__ inline int fwd_block_tiles(int m, int N, int N_k, int causal) {
+  const int r0 = m * kFwdRowsPerCta;
+  return fwd_kv_tile_end(r0, min(N, r0 + kFwdRowsPerCta), N_k, causal);
+}
+
+// CTAs of a split launch: sum over row blocks of their part counts, times B*H.
+inline long long fwd_split_ctas(int N, int N_k, int causal, int num_splits, int n_max, int BH) {
+  long long total = 0;
+  const int M = fwd_num_m_blocks(N);
+  for (int m = 0; m < M; ++m) total += fwd_num_parts(fwd_block_tiles(m, N, N_k, causal), num_splits, n_max);
+  return total * BH;
 }
 
 // The split count: for each candidate s in [1, min(max_splits, num_sms,
@@ -104,9 +129,12 @@ struct FwdArgs {
   int* tile_count;    // optional: per-CTA count of K/V tiles loaded (nullptr = off)
   unsigned long long timeout_ns;  // bound on every mbarrier wait
   int fault;          // 0 normally; 1 = producer skips the first V tile (failure-path test)
-  int num_splits;     // K/V parts per worker; <= 1: no split
+  int num_splits;     // K/V parts of the longest worker; <= 1: no split
+  int kv_tiles_max;   // split mode: K/V tile count of the longest row block
+  void* o;            // split mode: [B*H][N][d] 16-bit output, written by the merging group
   float* o_part;      // split mode: [num_splits][B*H][N][d] fp32 O / l of each part
   float* lse_part;    // split mode: [num_splits][B*H][N] fp32 logsumexp of each part (-inf: empty)
+  int* part_done;     // split mode: [B*H][num_m_blocks][2] arrivals per row tile, zero on entry
 };
 
 struct BwdArgs {

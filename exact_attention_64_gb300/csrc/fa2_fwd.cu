@@ -63,7 +63,130 @@ struct FwdShared {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
+  int work[4];  // split mode: row block, batch*head, part, part count
+  int merge[2];  // split mode: this CTA's row tile t arrived last and merges it
 };
+
+// Split mode: CTA `cta` of the 1-D grid -> (row block, batch*head, part, parts).
+// Row blocks are ranked longest first; rank k owns parts(k) * BH consecutive
+// CTAs, heads varying fastest, so that the long parts of every head start
+// before any short one. One warp scans 32 ranks at a time (inclusive prefix
+// sum of the CTA counts) and lane 0 of the hit writes the result.
+__device__ __forceinline__ void fwd_split_locate(int cta, int M, int N, int Nk, int causal, int S,
+                                                 int n_max, int BH, int lane, int* out) {
+  int base = 0;
+  for (int k0 = 0; k0 < M; k0 += 32) {
+    const int k = k0 + lane;
+    int m = 0, p = 0;
+    if (k < M) {
+      m = fwd_m_block_of(k, M, causal);
+      p = fwd_num_parts(fwd_block_tiles(m, N, Nk, causal), S, n_max);
+    }
+    const int c = p * BH;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, k < M && cta < base + incl);
+    if (hit != 0u) {
+      if (lane == __ffs(hit) - 1) {
+        const int r = cta - (base + incl - c);
+        out[0] = m;
+        out[1] = r % BH;
+        out[2] = r / BH;
+        out[3] = p;
+      }
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) out[0] = out[1] = out[2] = out[3] = 0;  // past the last part: no work
+}
+
+// Merge of a row tile's K/V parts, run by the warpgroup whose part arrived
+// last ("大猿搬砖简记", thread-block section: the partial results of the
+// blocks that share a worker's K/V range are combined to recover the global
+// softmax). Part s of a row holds O_s = (sum over its keys of exp(S - m_s) V)
+// / l_s and lse_s = m_s + ln l_s (-inf: no key of the part is visible); then
+//   L = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - L) O_s,
+// with O rounded once to the 16-bit type. Each warp merges its 32 rows: lane =
+// row forms L and the weights (staged in the warp's 4 KiB shared slice, 32
+// parts at a time, XOR-swizzled), then the lanes cover 4 rows x 32 columns per
+// load so that every read of the parts is a whole 128-byte segment. The parts
+// were written by other CTAs: they are read through L2 (ld.global.cg).
+template <int D, bool BF16>
+__device__ __forceinline__ void fwd_merge_rows(const FwdArgs& a, int bh, int wrow0, int parts,
+                                               int lane, float* wsm) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int N = a.N;
+  const size_t bhn = static_cast<size_t>(a.B) * a.H * N;
+  const size_t rbase = static_cast<size_t>(bh) * N;
+  const int my_row = wrow0 + lane;
+  const bool row_in = my_row < N;
+  float mx = -INFINITY;
+  if (row_in)
+    for (int s = 0; s < parts; ++s) mx = fmaxf(mx, __ldcg(a.lse_part + s * bhn + rbase + my_row));
+  float L = -INFINITY;
+  if (mx != -INFINITY) {
+    float tot = 0.f;
+    for (int s = 0; s < parts; ++s)
+      tot += ex2_approx((__ldcg(a.lse_part + s * bhn + rbase + my_row) - mx) * kLog2e);
+    L = mx + lg2_approx(tot) * kLn2;
+  }
+  if (row_in) a.lse[rbase + my_row] = L;
+  // Weights of parts [s0, s0 + 32) of this lane's row: wsm[row][k ^ row].
+  auto stage_weights = [&](int s0) {
+    __syncwarp();
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) {
+      const int s = s0 + k;
+      float w = 0.f;
+      if (s < parts && L != -INFINITY)
+        w = ex2_approx((__ldcg(a.lse_part + s * bhn + rbase + my_row) - L) * kLog2e);
+      wsm[lane * 32 + (k ^ lane)] = w;
+    }
+    __syncwarp();
+  };
+  const int sub = lane >> 3, seg = lane & 7;
+  const bool once = parts <= 32;
+  if (once) stage_weights(0);
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    float4 acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < parts; s0 += 32) {
+      if (!once) stage_weights(s0);
+      const int cnt = min(32, parts - s0);
+#pragma unroll 2
+      for (int k = 0; k < cnt; ++k) {
+        const float* src = a.o_part + ((s0 + k) * bhn + rbase) * D + c + seg * 4;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + sub;
+          if (wrow0 + rr < N) {
+            const float w = wsm[rr * 32 + (k ^ rr)];
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(wrow0 + rr) * D));
+            acc[i].x = fmaf(w, x.x, acc[i].x);
+            acc[i].y = fmaf(w, x.y, acc[i].y);
+            acc[i].z = fmaf(w, x.z, acc[i].z);
+            acc[i].w = fmaf(w, x.w, acc[i].w);
+          }
+        }
+      }
+    }
+    uint16_t* o16 = static_cast<uint16_t*>(a.o);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + sub;
+      if (wrow0 + rr < N)
+        *reinterpret_cast<uint2*>(o16 + (rbase + wrow0 + rr) * D + c + seg * 4) =
+            make_uint2(pack_x2<BF16>(acc[i].x, acc[i].y), pack_x2<BF16>(acc[i].z, acc[i].w));
+    }
+  }
+}
 
 // S_t = Q_t K^T : M=128 queries, N=128 keys, K=d. Both operands K-major,
 // 128-byte swizzled, one 64-element slab per 16 KiB. Issued by a converged
@@ -114,24 +237,7 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;    // queries
   const int Nk = a.Nk;  // keys and values
-  // grid = (m block x K/V part, batch, head); without a split there is one part.
   const int S = a.num_splits > 1 ? a.num_splits : 1;
-  const int split = blockIdx.x % S;
-  const int mb = fwd_m_block_of(blockIdx.x / S, a.num_m_blocks, CAUSAL);
-  const int bh = blockIdx.y * a.H + blockIdx.z;
-  const int row0 = mb * kFwdRowsPerCta;
-  const int rows_a = min(kTileRows, N - row0);
-  const int rows_b = max(0, min(kTileRows, N - row0 - kTileRows));
-  const int end_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, Nk, CAUSAL),
-                        fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, Nk, CAUSAL)};
-  // This CTA's part [kv_lo, kv_hi) of the K/V tiles. Below, j counts tiles
-  // within the part (ring slots, phases, first-tile flags); kv_lo + j is the
-  // K/V tile itself (TMA coordinates, masks).
-  int kv_lo, kv_hi;
-  fwd_split_range(max(end_t[0], end_t[1]), S, split, &kv_lo, &kv_hi);
-  const int n_t[2] = {max(0, min(kv_hi, end_t[0]) - kv_lo), max(0, min(kv_hi, end_t[1]) - kv_lo)};
-  const int n_total = max(n_t[0], n_t[1]);
-
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
     for (int i = 0; i < C::NK; ++i) { mbar_init(&sh.k_full[i], 1); mbar_init(&sh.k_empty[i], 1); }
@@ -149,9 +255,30 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
+  if (S > 1 && warp == 2)
+    fwd_split_locate(blockIdx.x, a.num_m_blocks, N, Nk, CAUSAL, S, a.kv_tiles_max, a.B * a.H, lane,
+                     sh.work);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Without a split the grid is (row block, batch, head) with one part per
+  // block; with one it is 1-D and the locator above placed this CTA.
+  const int mb = S > 1 ? sh.work[0] : fwd_m_block_of(blockIdx.x, a.num_m_blocks, CAUSAL);
+  const int bh = S > 1 ? sh.work[1] : blockIdx.y * a.H + blockIdx.z;
+  const int split = S > 1 ? sh.work[2] : 0;
+  const int parts = S > 1 ? sh.work[3] : 1;
+  const int row0 = mb * kFwdRowsPerCta;
+  const int rows_a = min(kTileRows, N - row0);
+  const int rows_b = max(0, min(kTileRows, N - row0 - kTileRows));
+  const int end_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, Nk, CAUSAL),
+                        fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, Nk, CAUSAL)};
+  // This CTA's part [kv_lo, kv_hi) of the block's K/V tiles. Below, j counts
+  // tiles within the part (ring slots, phases, first-tile flags); kv_lo + j is
+  // the K/V tile itself (TMA coordinates, masks).
+  int kv_lo, kv_hi;
+  fwd_part_range(max(end_t[0], end_t[1]), parts, split, &kv_lo, &kv_hi);
+  const int n_t[2] = {max(0, min(kv_hi, end_t[0]) - kv_lo), max(0, min(kv_hi, end_t[1]) - kv_lo)};
+  const int n_total = max(n_t[0], n_t[1]);
   const uint32_t tmem = sh.tmem_base;
   volatile int* abort_flag = &sh.abort_flag;
   const WaitCtx wc{a.status, abort_flag, a.timeout_ns};
@@ -357,39 +484,83 @@ __global__ void __launch_bounds__(384, 1)
     }
     // ---------------- epilogue: O / l -> 16-bit, L = m + ln l ----------------
     if (ok && nt > 0) ok = mbar_wait_warp(&sh.o_full[t], (nt - 1) & 1, wc);
-    if (a.o_part != nullptr) {
+    if (a.o_part != nullptr && parts > 1) {
       // K/V split: this part's O / l in fp32 and its logsumexp, for the merge
-      // pass; an empty part contributes O = 0 with logsumexp -inf. The TMEM
+      // pass; a part with no key of this tile's rows (causal: the part lies
+      // past them) contributes O = 0 with logsumexp -inf. A block with a single
+      // part takes the plain epilogue below and writes O and L itself. The TMEM
       // loads are warp-collective: the whole warp runs them, and only the
       // stores are limited to rows inside the sequence.
+      // Global stores are made whole 128-byte row segments: each warp passes
+      // its 32 rows x 32 columns through a private 4 KiB slice of Q_t's shared
+      // buffer (free once Q_t's last product has completed), 16-byte chunks
+      // XOR-swizzled by row so that neither side conflicts on banks.
       const bool row_in = my_row < N;
-      const size_t prow = static_cast<size_t>(split) * (static_cast<size_t>(a.B) * a.H) * N +
-                          static_cast<size_t>(bh) * N + (row_in ? my_row : 0);
-      float4* dst = reinterpret_cast<float4*>(a.o_part + prow * D);
+      const size_t part_base =
+          (static_cast<size_t>(split) * (static_cast<size_t>(a.B) * a.H) + bh) * static_cast<size_t>(N);
+      const int wrow0 = row_base + quad * 32;  // first row of this warp
+      const int sub = lane >> 3, seg = lane & 7;  // store phase: 4 rows x 8 chunks of 16 bytes
       if (ok && nt > 0) {
         __syncwarp();
         tc_fence_after();
         const float inv_l = 1.f / l;
-#pragma unroll
+        float4* slice = reinterpret_cast<float4*>(smem + C::OFF_Q + t * C::TILE_BYTES + quad * 4096);
+#pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
           tmem_ld_32x32b_x32(t_o + c, o);
           tmem_wait_ld();
           reg_fence(o);
-          if (row_in) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[c / 4 + k] = make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                                           __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+          for (int k = 0; k < 8; ++k)
+            slice[lane * 8 + (k ^ (lane & 7))] =
+                make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
+                            __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + sub;
+            const float4 val = slice[rr * 8 + (seg ^ (rr & 7))];
+            if (wrow0 + rr < N)
+              reinterpret_cast<float4*>(a.o_part + (part_base + wrow0 + rr) * D + c)[seg] = val;
+          }
+          __syncwarp();
+        }
+        if (row_in) a.lse_part[part_base + my_row] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
+      } else if (ok) {
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + sub;
+            if (wrow0 + rr < N)
+              reinterpret_cast<float4*>(a.o_part + (part_base + wrow0 + rr) * D + c)[seg] = zero;
           }
         }
-        if (row_in) a.lse_part[prow] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
-      } else if (ok && row_in) {
-#pragma unroll
-        for (int k = 0; k < D / 4; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        a.lse_part[prow] = -INFINITY;
+        if (row_in) a.lse_part[part_base + my_row] = -INFINITY;
       }
-      named_bar_sync(1 + t, 128);  // as below: every warp of the group reaches it
+      // Arrival on the row tile's part counter: every thread's stores are made
+      // visible device-wide first; the group whose arrival completes the
+      // count merges the parts. Nothing waits on another CTA. Every warp of
+      // the group reaches both barriers on every path, aborted or not.
+      __threadfence();
+      named_bar_sync(1 + t, 128);
+      if ((threadIdx.x & 127) == 0) {
+        const size_t ci = (static_cast<size_t>(bh) * a.num_m_blocks + mb) * 2 + t;
+        sh.merge[t] = atomicAdd(a.part_done + ci, 1) == parts - 1;
+      }
+      named_bar_sync(1 + t, 128);
+      if (sh.merge[t]) {
+        // The merge stages its weights in Q_t's buffer. A group with no key in
+        // this part skipped every wait, so Q's copy may still be landing there.
+        bool q_in = true;
+        if (nt == 0 && n_total > 0) q_in = mbar_wait_warp(&sh.q_full, 0, wc);
+        __threadfence();
+        if (q_in)
+          fwd_merge_rows<D, BF16>(a, bh, wrow0, parts, lane,
+                                  reinterpret_cast<float*>(smem + C::OFF_Q + t * C::TILE_BYTES + quad * 4096));
+      }
     } else {
       // Q_t's shared buffer is free (its last S product has completed): stage O
       // there in the same 128-byte-swizzled layout and store it with TMA, which
@@ -450,7 +621,12 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   auto kern = fa2_fwd_kernel<D, BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_m_blocks * (a.num_splits > 1 ? a.num_splits : 1), a.B, a.H);
+  dim3 grid(a.num_m_blocks, a.B, a.H);
+  if (a.num_splits > 1) {
+    const long long ctas = fwd_split_ctas(a.N, a.Nk, CAUSAL, a.num_splits, a.kv_tiles_max, a.B * a.H);
+    if (ctas < 1 || ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    grid = dim3(static_cast<unsigned>(ctas), 1, 1);
+  }
   kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }

@@ -77,10 +77,15 @@ int fa2_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
 /* K/V-split forward ("大猿搬砖简记", thread-block section: when the (row block,
  * batch, head) workers cannot fill the SMs, each worker's K/V range may be cut
  * into num_splits parts run by separate blocks, whose partial results are then
- * combined to recover the global softmax). Part s of a worker covers
- * ceil(tiles / num_splits) of its K/V tiles of 128 keys (the last parts shorter
- * or empty); each part writes its fp32 O / l and logsumexp into the workspace,
- * and a merge pass forms L = ln sum_s exp(lse_s), O = sum_s exp(lse_s - L) O_s.
+ * combined to recover the global softmax). num_splits is the part count of the
+ * longest worker (n_max K/V tiles of 128 keys); a worker with n tiles (shorter
+ * under the causal mask) gets min(n, ceil(n * num_splits / n_max)) balanced,
+ * contiguous, non-empty parts. A worker with one part writes O and L itself;
+ * the parts of the others write fp32 O / l and logsumexp into the workspace
+ * and count their arrival per 128-row tile; the part that arrives last forms
+ * L = ln sum_s exp(lse_s), O = sum_s exp(lse_s - L) O_s (no CTA waits on
+ * another; the counters are zeroed on the stream before the launch). Blocks
+ * are launched longest row block first, heads varying fastest.
  * Same result as fa2_fwd up to rounding.
  *   num_splits : 1 .. 128 (1 runs fa2_fwd and ignores the workspace).
  *   workspace  : device, >= fa2_fwd_split_workspace_size(...) bytes, 256-byte
@@ -91,8 +96,10 @@ int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* l
                   int N, int d, int causal, float scale, int dtype, int num_splits, void* workspace,
                   size_t workspace_bytes, void* stream);
 
-/* Bytes of workspace fa2_fwd_split needs: num_splits x B*H x N x (d + 1) fp32,
- * each of the two arrays rounded up to 256 bytes. Returns 0 for invalid sizes. */
+/* Bytes of workspace fa2_fwd_split needs: num_splits x B*H x N x (d + 1) fp32
+ * (the parts' O / l and logsumexp) plus B*H x ceil(N / 256) x 2 int32 arrival
+ * counters, each of the three arrays rounded up to 256 bytes. Returns 0 for
+ * invalid sizes. */
 size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /* The split count of the same page: for each candidate s in 1 .. min(128,

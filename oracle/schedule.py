@@ -42,7 +42,8 @@ __all__ = [
     "bwd_q_tile_range",
     "split_utilisation",
     "num_splits_heuristic",
-    "split_kv_range",
+    "split_num_parts",
+    "split_part_range",
 ]
 
 
@@ -133,12 +134,21 @@ def num_splits_heuristic(workers: int, num_sms: int, num_n_blocks: int, max_spli
     return 1
 
 
-def split_kv_range(j_begin: int, j_end: int, num_splits: int, split: int):
-    """Part `split` of a worker's K/V tile range [j_begin, j_end) cut into
-    `num_splits` contiguous parts of ceil(len / num_splits) tiles each (the
-    last parts shorter or empty)."""
-    n = max(0, j_end - j_begin)
-    per = ceil_div(n, num_splits) if n else 0
-    lo = min(j_begin + split * per, j_end) if n else j_begin
-    hi = min(lo + per, j_end) if n else j_begin
-    return (lo, hi)
+def split_num_parts(n: int, num_splits: int, n_max: int) -> int:
+    """Part count of a worker with n K/V tiles when the longest worker (n_max
+    tiles) is cut into num_splits parts: proportionally fewer for a shorter
+    range, min(n, ceil(n * num_splits / n_max)), never an empty part. Reading
+    of the page's split paragraph, which gives the part count of a worker but
+    not how unequal (causal) workers share it."""
+    if n <= 0:
+        return 0
+    if num_splits <= 1:
+        return 1
+    return min(n, ceil_div(n * num_splits, n_max))
+
+
+def split_part_range(j_begin: int, j_end: int, parts: int, part: int):
+    """Part `part` of `parts` contiguous, balanced parts of the tile range
+    [j_begin, j_end): lengths floor or ceil of len / parts, in order."""
+    n = j_end - j_begin
+    return (j_begin + part * n // parts, j_begin + (part + 1) * n // parts)

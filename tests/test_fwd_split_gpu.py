@@ -83,3 +83,30 @@ def test_fwd_split_rejects_bad_split_counts(cuda_device, fa2_lib):
     assert lib.fa2_fwd_split(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(),
                              lse.data_ptr(), 1, 1, 128, 64, 0, 0.125, 1, 4, ws.data_ptr(), 16,
                              None) == 7
+
+
+def test_fwd_split_reuses_a_dirty_workspace(cuda_device, fa2_lib):
+    """The workspace's contents are ignored on entry: a buffer full of garbage,
+    then the same buffer again (arrival counters left at their final values),
+    give the same bits as a fresh run."""
+    B, H, N, d, S = 1, 2, 1000, 128, 5
+    q, k, v, _ = make_inputs(B, H, N, d, torch.bfloat16, seed=77)
+    qd, kd, vd = (t.to(cuda_device) for t in (q, k, v))
+    lib = fa2_lib.load_library()
+    nbytes = lib.fa2_fwd_split_workspace_size(B, H, N, d, S)
+    ws = torch.full((nbytes,), 0x5A, dtype=torch.uint8, device=cuda_device)
+    outs = []
+    for _ in range(2):
+        o = torch.empty_like(qd)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=cuda_device)
+        code = lib.fa2_fwd_split(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, d, 1, 1.0 / math.sqrt(d), 1, S,
+                                 ws.data_ptr(), nbytes, None)
+        assert code == 0
+        torch.cuda.synchronize()
+        outs.append((o.cpu(), lse.cpu()))
+    assert fa2_lib.device_status() == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    o_ref, lse_ref = oracle_fwd(q, k, v, True, 1.0 / math.sqrt(d))
+    assert max_abs(to64(outs[0][0]), o_ref) <= TOL[torch.bfloat16]["o"]
+    assert max_abs(to64(outs[0][1]), lse_ref) <= TOL[torch.bfloat16]["lse"]

@@ -75,6 +75,8 @@ def test_split_workspace_size(fa2_lib):
 
     for B, H, N, d, S in ((1, 2, 16384, 128, 7), (2, 3, 1000, 64, 3), (1, 1, 1, 64, 1)):
         rows = S * B * H * N
-        assert lib.fa2_fwd_split_workspace_size(B, H, N, d, S) == up(rows * d * 4) + up(rows * 4)
+        counters = B * H * (-(-N // 256)) * 2 * 4
+        assert (lib.fa2_fwd_split_workspace_size(B, H, N, d, S)
+                == up(rows * d * 4) + up(rows * 4) + up(counters))
     assert lib.fa2_fwd_split_workspace_size(1, 1, 128, 128, 0) == 0
     assert lib.fa2_fwd_split_workspace_size(1, 1, 128, 128, 129) == 0

@@ -100,15 +100,46 @@ def test_num_splits_follows_the_stated_rule():
             assert all(eff[c - 1] < 0.95 * max(eff) for c in range(1, s))
 
 
-@pytest.mark.parametrize("j0,j1", [(0, 0), (0, 1), (0, 5), (3, 17), (0, 128)])
-def test_split_kv_range_partitions_the_range(j0, j1):
-    for S in range(1, 9):
-        parts = [schedule.split_kv_range(j0, j1, S, s) for s in range(S)]
+@pytest.mark.parametrize("j0,j1", [(0, 1), (0, 5), (3, 17), (0, 128)])
+def test_split_part_range_partitions_the_range(j0, j1):
+    for p in range(1, j1 - j0 + 1):
+        parts = [schedule.split_part_range(j0, j1, p, s) for s in range(p)]
         covered = [j for lo, hi in parts for j in range(lo, hi)]
         assert covered == list(range(j0, j1))  # disjoint, in order, complete
-        per = schedule.ceil_div(j1 - j0, S) if j1 > j0 else 0
-        assert all(hi - lo <= per for lo, hi in parts)
-        assert all(j0 <= lo <= hi <= j1 for lo, hi in parts)
+        lens = [hi - lo for lo, hi in parts]
+        assert min(lens) >= 1 and max(lens) - min(lens) <= 1
+
+
+def test_split_num_parts_rule():
+    """The longest worker gets num_splits parts (fewer only if it has fewer
+    tiles); shorter workers get no more, none gets an empty part, and no part
+    of any worker is longer than ceil(n_max / num_splits) tiles."""
+    for n_max in (1, 2, 7, 19, 64, 128):
+        for S in range(1, 20):
+            assert schedule.split_num_parts(n_max, S, n_max) == min(S, n_max)
+            cap = schedule.ceil_div(n_max, S)
+            prev = 0
+            for n in range(1, n_max + 1):
+                p = schedule.split_num_parts(n, S, n_max)
+                assert 1 <= p <= min(n, S) and p >= prev
+                prev = p
+                longest = max(hi - lo for lo, hi in
+                              (schedule.split_part_range(0, n, p, s) for s in range(p)))
+                assert longest <= cap
+    assert schedule.split_num_parts(0, 7, 128) == 0
+    assert schedule.split_num_parts(5, 1, 128) == 1
+
+
+def test_split_parts_of_the_two_head_long_sequence():
+    """B=1 H=2 N=16384 causal, 7 splits: 256-row block m has 2m+2 tiles of 128
+    keys (n_max = 128). Counted by hand from the thresholds p = k for
+    128(k-1)/7 < 2m+2 <= 128k/7: nine even tile counts in each of the first
+    six intervals (2..18, 20..36, ..., 92..108) and ten in the last
+    (110..128), 9*(1+...+6) + 7*10 = 259 parts per head."""
+    counts = [schedule.split_num_parts(2 * m + 2, 7, 128) for m in range(64)]
+    by_k = {k: counts.count(k) for k in range(1, 8)}
+    assert by_k == {1: 9, 2: 9, 3: 9, 4: 9, 5: 9, 6: 9, 7: 10}
+    assert sum(counts) == 259
 
 
 @pytest.mark.parametrize("N,Nk", [(1, 300), (300, 1), (130, 500), (500, 130), (256, 257)])
