@@ -412,7 +412,8 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": (5 if fwd_splits > 1 else 4) * args.steps,  # + the merge pass when split
+        # fwd, bwd pre, dK/dV, dQ per step (a split forward adds a counter memset, not a kernel)
+        "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:
