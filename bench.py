@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--cpu-sample-heads", type=int, default=3)
     p.add_argument("--fwd-splits", default="1",
                    help="K/V parts per forward worker: an integer or 'auto' (fa2_fwd_split)")
+    p.add_argument("--fwd-order", default="fa2", choices=["fa2", "kv_outer"],
+                   help="forward loop order: fa2 (Q outer) or kv_outer (the FlashAttention-1 "
+                        "order, fa2_fwd_kv_outer), for measuring the loop order")
     return p.parse_args()
 
 
@@ -242,8 +245,18 @@ def main():
     split_bytes = lib.fa2_fwd_split_workspace_size(B, H, N, d, fwd_splits) if fwd_splits > 1 else 0
     split_ws = torch.empty(max(split_bytes, 1), dtype=torch.uint8, device=dev)
 
+    kv_outer = args.fwd_order == "kv_outer"
+    if kv_outer and fwd_splits > 1:
+        raise SystemExit("--fwd-order kv_outer takes no K/V split")
+    fa1_bytes = lib.fa2_fwd_kv_outer_workspace_size(B, H, N, d) if kv_outer else 0
+    fa1_ws = torch.empty(max(fa1_bytes, 1), dtype=torch.uint8, device=dev)
+
     def fwd():
-        if fwd_splits > 1:
+        if kv_outer:
+            c = lib.fa2_fwd_kv_outer(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), B, H, N, d, causal, scale, dt_code,
+                                     fa1_ws.data_ptr(), fa1_bytes, sp)
+        elif fwd_splits > 1:
             c = lib.fa2_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                   lse.data_ptr(), B, H, N, d, causal, scale, dt_code, fwd_splits,
                                   split_ws.data_ptr(), split_bytes, sp)
@@ -326,7 +339,7 @@ def main():
     # not count, so only one unit is credited to it.
     fw = w.fwd_flops()
     kernels = {
-        "fa2_fwd_kernel": (mean(t_fwd), fw, "tensor"),
+        ("fa1_order_fwd_kernel" if kv_outer else "fa2_fwd_kernel"): (mean(t_fwd), fw, "tensor"),
         "fa2_bwd_dkdv_kernel": (mean(t_kv), 2.0 * fw, "tensor"),
         "fa2_bwd_dq_kernel": (mean(t_dq), 0.5 * fw, "tensor"),
         "fa2_bwd_pre_kernel": (mean(t_pre), B * H * N * (2 * d * 2 + 4 + 8), "hbm"),
@@ -404,7 +417,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "q_std": w.q_std, "parallelism": f"head-sharded replicas x{world}",
-                   "l2": l2_note, "fwd_splits": fwd_splits},
+                   "l2": l2_note, "fwd_splits": fwd_splits, "fwd_order": args.fwd_order},
         "detail": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
                    "fwd_frac_of_peak": fwd_tf / pk["bf16_sustained"],
                    "bwd_frac_of_peak": bwd_tf / pk["bf16_sustained"],

@@ -24,6 +24,7 @@ __all__ = [
     "load_library",
     "forward",
     "forward_instrumented",
+    "forward_kv_outer",
     "backward",
     "bwd_workspace_size",
     "device_status",
@@ -71,6 +72,8 @@ def load_library() -> ctypes.CDLL:
         "fa2_fwd_qk": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]),
         "fa2_bwd_qk": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp, sz, vp]),
         "fa2_fwd_split_workspace_size": (sz, [i, i, i, i, i]),
+        "fa2_fwd_kv_outer": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]),
+        "fa2_fwd_kv_outer_workspace_size": (sz, [i, i, i, i]),
         "fa2_num_splits": (i, [i, i, i, i, i, i]),
         "fa2_bwd_workspace_size": (sz, [i, i, i, i]),
         "fa2_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]),
@@ -183,6 +186,34 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     code = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, d, int(bool(causal)), float(scale), _DTYPES[dt], _stream_ptr(dev))
     _check("fa2_fwd", code)
+    return out, lse
+
+
+def forward_kv_outer(q, k, v, causal: bool = False, scale: float | None = None):
+    """The same (o, lse) as ``forward``, computed in the FlashAttention-1 loop
+    order (fa2_fwd_kv_outer: K/V blocks outer, the running O, m, l of every
+    query block read from and written back to HBM at each step). For
+    measuring the loop order; ``forward`` is the fast path."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise ValueError("q must be float16 or bfloat16")
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_tensor(name, t, (B, H, N, d), dt, dev)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lib = load_library()
+    nbytes = lib.fa2_fwd_kv_outer_workspace_size(B, H, N, d)
+    if nbytes == 0:
+        raise FA2Error("fa2_fwd_kv_outer_workspace_size", 1)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    code = lib.fa2_fwd_kv_outer(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                _DTYPES[dt], ws.data_ptr(), nbytes, _stream_ptr(dev))
+    _check("fa2_fwd_kv_outer", code)
     return out, lse
 
 

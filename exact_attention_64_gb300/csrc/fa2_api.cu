@@ -16,6 +16,9 @@ namespace fa2 {
 cudaError_t launch_fwd(int d, bool bf16, bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, const FwdArgs& a,
                        cudaStream_t stream);
+cudaError_t launch_fa1_order_fwd(int d, bool bf16, bool causal, const CUtensorMap& tq,
+                                 const CUtensorMap& tk, const CUtensorMap& tv, const Fa1Args& a,
+                                 cudaStream_t stream);
 cudaError_t launch_bwd(int d, bool bf16, bool causal, const void* o, const void* dO,
                        const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
                        float* l2, cudaStream_t stream, cudaEvent_t* ev);
@@ -264,6 +267,63 @@ int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* l
   if (num_splits < 1 || num_splits > kMaxFwdSplits) return FA2_ERR_INVALID_ARG;
   return fwd_impl(q, k, v, o, lse, B, H, N, N, d, causal, scale, dtype, nullptr, stream, num_splits,
                   workspace, workspace_bytes);
+}
+
+size_t fa2_fwd_kv_outer_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  // [O_i: B*H x N x d fp32][m_i: B*H x N fp32][l_i: B*H x N fp32]
+  const size_t rows = static_cast<size_t>(B) * H * N;
+  return align_up(rows * d * 4, 256) + 2 * align_up(rows * 4, 256);
+}
+
+int fa2_fwd_kv_outer(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, int causal, float scale, int dtype, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA2_ERR_INVALID_ARG;
+  int st = check_common(B, H, N, d, causal, scale, dtype);
+  if (st != FA2_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return FA2_ERR_ALIGNMENT;
+  const size_t need = fa2_fwd_kv_outer_workspace_size(B, H, N, d);
+  if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return FA2_ERR_ALIGNMENT;
+  const size_t tbytes = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t lbytes = static_cast<size_t>(B) * H * N * 4;
+  const void* ins[3] = {q, k, v};
+  for (int x = 0; x < 3; ++x)
+    if (overlap(o, tbytes, ins[x], tbytes) || overlap(lse, lbytes, ins[x], tbytes) ||
+        overlap(workspace, need, ins[x], tbytes))
+      return FA2_ERR_OVERLAP;
+  if (overlap(o, tbytes, lse, lbytes) || overlap(workspace, need, o, tbytes) ||
+      overlap(workspace, need, lse, lbytes))
+    return FA2_ERR_OVERLAP;
+  int dev = 0;
+  int* status = nullptr;
+  st = device_setup(&dev, &status);
+  if (st != FA2_OK) return st;
+  const int BH = B * H;
+  CUtensorMap tq, tk, tv;
+  if (make_map_16bit(&tq, q, BH, N, d, dtype) || make_map_16bit(&tk, k, BH, N, d, dtype) ||
+      make_map_16bit(&tv, v, BH, N, d, dtype))
+    return FA2_ERR_CUDA;
+  const size_t rows = static_cast<size_t>(BH) * N;
+  char* ws = static_cast<char*>(workspace);
+  fa2::Fa1Args a{};
+  a.o = o;
+  a.lse = lse;
+  a.o_acc = reinterpret_cast<float*>(ws);
+  a.m_acc = reinterpret_cast<float*>(ws + align_up(rows * d * 4, 256));
+  a.l_acc = reinterpret_cast<float*>(ws + align_up(rows * d * 4, 256) + align_up(rows * 4, 256));
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.status = status;
+  a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
+  (void)cudaGetLastError();
+  const cudaError_t e = fa2::launch_fa1_order_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, a,
+                                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA2_OK : cuda_fail(e);
 }
 
 int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, float* lse, int B,

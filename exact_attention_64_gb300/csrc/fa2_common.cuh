@@ -137,6 +137,19 @@ struct FwdArgs {
   int* part_done;     // split mode: [B*H][num_m_blocks][2] arrivals per row tile, zero on entry
 };
 
+// Argument block of the K/V-outer (FlashAttention-1 order) forward kernel.
+struct Fa1Args {
+  void* o;            // [B*H][N][d] 16-bit output
+  float* lse;         // [B*H][N] natural-log logsumexp
+  float* o_acc;       // workspace [B*H][N][d] fp32: running O_i (normalised)
+  float* m_acc;       // workspace [B*H][N] fp32: running max (scaled, log2 units)
+  float* l_acc;       // workspace [B*H][N] fp32: running sum
+  int B, H, N;
+  float scale_log2;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
 struct BwdArgs {
   const float* l2_pad;    // L * log2(e), [B*H, n_pad] fp32 (0 past row N)
   const float* dsum_pad;  // D = rowsum(dO o O), [B*H, n_pad] fp32 (0 past row N)

@@ -96,6 +96,28 @@ int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* l
                   int N, int d, int causal, float scale, int dtype, int num_splits, void* workspace,
                   size_t workspace_bytes, void* stream);
 
+/* Forward pass in the FlashAttention-1 loop order, for measuring the loop
+ * order ("FlashAttention学习笔记(2)", the FlashAttention-1 forward algorithm
+ * and the comparison of the two loop orders): K/V blocks outer, query blocks
+ * inner, one CTA per (batch, head). At every (K/V block j, query block i) step
+ * the running O_i (kept normalised), row max m_i and row sum l_i are read from
+ * and written back to the workspace in HBM:
+ *   m_new = max(m_i, m~), l_new = e^(m_i - m_new) l_i + e^(m~ - m_new) l~,
+ *   O_i <- (l_i e^(m_i - m_new) O_i + e^(m~ - m_new) P~ V_j) / l_new,
+ * with m~, P~ = exp(S - m~), l~ of the block S = scale Q_i K_j^T. The same
+ * O and L as fa2_fwd up to rounding. Query and key lengths are equal.
+ *   workspace : device, >= fa2_fwd_kv_outer_workspace_size(...) bytes,
+ *               256-byte aligned, scratch owned by the caller (contents
+ *               ignored on entry, undefined on exit).
+ *   other arguments as in fa2_fwd. */
+int fa2_fwd_kv_outer(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, int causal, float scale, int dtype, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace fa2_fwd_kv_outer needs: B*H x N x (d + 2) fp32 (O_i, m_i,
+ * l_i), each array rounded up to 256 bytes. Returns 0 for invalid sizes. */
+size_t fa2_fwd_kv_outer_workspace_size(int B, int H, int N, int d);
+
 /* Bytes of workspace fa2_fwd_split needs: num_splits x B*H x N x (d + 1) fp32
  * (the parts' O / l and logsumexp) plus B*H x ceil(N / 256) x 2 int32 arrival
  * counters, each of the three arrays rounded up to 256 bytes. Returns 0 for

@@ -103,3 +103,23 @@ def test_fault_arming_validates(fa2_lib):
     assert lib.fa2_debug_arm_fault(1, 0) == 1
     assert lib.fa2_debug_arm_fault(1, 10) == 0
     assert lib.fa2_debug_arm_fault(0, 0) == 0   # disarm again
+
+
+def test_kv_outer_rejects_bad_arguments(fa2_lib):
+    lib = fa2_lib.load_library()
+    ws = lib.fa2_fwd_kv_outer_workspace_size(1, 1, 128, 64)
+    base = [A + i * STEP for i in range(6)]
+
+    def call(ptrs=base, wsz=ws, d=64, causal=0):
+        p = list(ptrs)
+        return lib.fa2_fwd_kv_outer(p[0], p[1], p[2], p[3], p[4], 1, 1, 128, d, causal, 0.125, 1,
+                                    p[5], wsz, None)
+
+    assert call([0] + base[1:]) == 1
+    assert call(causal=3) == 1
+    assert call(d=80) == 2
+    assert call(wsz=ws - 1) == 7
+    assert call(base[:5] + [0]) == 7
+    assert call(base[:5] + [base[5] + 16]) == 3   # workspace must be 256-byte aligned
+    assert call(base[:3] + [base[0]] + base[4:]) == 8  # o aliases q
+    assert call(base[:5] + [base[1]]) == 8             # workspace overlaps k

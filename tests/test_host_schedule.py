@@ -80,3 +80,16 @@ def test_split_workspace_size(fa2_lib):
                 == up(rows * d * 4) + up(rows * 4) + up(counters))
     assert lib.fa2_fwd_split_workspace_size(1, 1, 128, 128, 0) == 0
     assert lib.fa2_fwd_split_workspace_size(1, 1, 128, 128, 129) == 0
+
+
+def test_kv_outer_workspace_size(fa2_lib):
+    lib = fa2_lib.load_library()
+
+    def up(x):
+        return -(-x // 256) * 256
+
+    for B, H, N, d in ((4, 32, 8192, 128), (2, 3, 1000, 64), (1, 1, 1, 64)):
+        rows = B * H * N
+        assert lib.fa2_fwd_kv_outer_workspace_size(B, H, N, d) == up(rows * d * 4) + 2 * up(rows * 4)
+    assert lib.fa2_fwd_kv_outer_workspace_size(1, 1, 128, 96) == 0
+    assert lib.fa2_fwd_kv_outer_workspace_size(0, 1, 128, 64) == 0
