@@ -48,6 +48,10 @@ def parse():
     p.add_argument("--cpu-sample-heads", type=int, default=3)
     p.add_argument("--fwd-splits", default="1",
                    help="K/V parts per forward worker: an integer or 'auto' (fa2_fwd_split)")
+    p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
+                   help="write profiles/traffic.json from an ncu report of --workload "
+                        "(dram__bytes_read.sum + dram__bytes_write.sum per kernel launch, scaled "
+                        "to the headline workload by heads) and exit")
     p.add_argument("--fwd-order", default="fa2", choices=["fa2", "kv_outer"],
                    help="forward loop order: fa2 (Q outer) or kv_outer (the FlashAttention-1 "
                         "order, fa2_fwd_kv_outer), for measuring the loop order")
@@ -192,6 +196,62 @@ def run_reference(args, w, rank, world):
     print(json.dumps(line), flush=True)
 
 
+TRAFFIC_FILES = {
+    "fa2_fwd_kernel": ["fa2_fwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_dkdv_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_dq_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_pre_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+}
+
+
+def record_traffic(rep: str, measured) -> None:
+    """profiles/traffic.json from one ncu capture of `measured` (one launch per
+    kernel): DRAM bytes read + written per launch, scaled to the headline
+    workload by the heads processed (same sequence length: each kernel reads its
+    inputs once and writes its outputs once, so traffic grows with B*H), with
+    the hash of the kernel's sources at the time of the capture."""
+    import csv
+    import io
+
+    from exact_attention_64_gb300.workloads import HEADLINE, WORKLOADS
+
+    head = WORKLOADS[HEADLINE]
+    if (measured.N, measured.d, measured.causal) != (head.N, head.d, head.causal):
+        raise SystemExit("the measured workload must share the headline's N, d and mask")
+    factor = (head.B * head.H) / (measured.B * measured.H)
+    text = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], capture_output=True,
+                          text=True, check=True).stdout
+    rows = list(csv.reader(io.StringIO(text)))
+    hdr, units, data = rows[0], rows[1], rows[2:]
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
+
+    def col(row, name):
+        i = hdr.index(name)
+        return float(row[i]) * scale[units[i]]
+
+    kernels = {}
+    for row in data:
+        name = row[hdr.index("Kernel Name")].split("(")[0].split("<")[0].split()[-1]
+        if name not in TRAFFIC_FILES or name in kernels:
+            continue
+        rd, wr = col(row, "dram__bytes_read.sum"), col(row, "dram__bytes_write.sum")
+        kernels[name] = {
+            "workload": head.name,
+            "bytes_per_launch": int(round((rd + wr) * factor)),
+            "measured": {"workload": measured.name, "dram_read_bytes": int(round(rd)),
+                         "dram_write_bytes": int(round(wr))},
+            "source_sha": source_sha(TRAFFIC_FILES[name]),
+            "files": TRAFFIC_FILES[name],
+        }
+    note = (f"dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture of "
+            f"{measured.name} (B={measured.B} H={measured.H}), scaled to {head.name} by the heads "
+            f"processed (x{factor:g}): each kernel reads its inputs from DRAM once and writes its "
+            f"outputs once, so traffic grows with B*H at fixed N. Written by "
+            f"`python bench.py --workload {measured.name} --record-traffic <report>`.")
+    PROFILE_TRAFFIC.write_text(json.dumps({"note": note, "kernels": kernels}, indent=1) + "\n")
+    print(json.dumps({k: v["bytes_per_launch"] for k, v in kernels.items()}))
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -201,6 +261,8 @@ def main():
     from exact_attention_64_gb300.workloads import HEADLINE, WORKLOADS
 
     w = WORKLOADS[args.workload or HEADLINE]
+    if args.record_traffic:
+        return record_traffic(args.record_traffic, w)
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
     if args.warmup < 3:
