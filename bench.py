@@ -52,6 +52,8 @@ def parse():
                    help="write profiles/traffic.json from an ncu report of --workload "
                         "(dram__bytes_read.sum + dram__bytes_write.sum per kernel launch, scaled "
                         "to the headline workload by heads) and exit")
+    p.add_argument("--e2e-heads-per-chunk", type=int, default=0,
+                   help="heads per pipelined chunk of the end-to-end leg (fa2_step_host; 0 = auto)")
     p.add_argument("--fwd-order", default="fa2", choices=["fa2", "kv_outer"],
                    help="forward loop order: fa2 (Q outer) or kv_outer (the FlashAttention-1 "
                         "order, fa2_fwd_kv_outer), for measuring the loop order")
@@ -440,13 +442,19 @@ def main():
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
         d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
 
+        hpc = args.e2e_heads_per_chunk
+        e2e_ws_bytes = lib.fa2_step_host_workspace_size(B, H, N, d, hpc)
+        e2e_ws = torch.empty(e2e_ws_bytes, dtype=torch.uint8, device=dev)
+
         def e2e_step():
-            for hsrc, ddst in ((hq, q), (hk, k), (hv, v), (hdo, do)):
-                ddst.copy_(hsrc, non_blocking=True)
-            fwd()
-            bwd()
-            for dsrc, hdst in ((o, ho), (lse, hlse), (dq, hdq), (dk, hdk), (dv, hdv)):
-                hdst.copy_(dsrc, non_blocking=True)
+            # One call of the public host-buffer entry point: uploads, kernels
+            # and downloads of the step, pipelined by head chunks.
+            c = lib.fa2_step_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hdo.data_ptr(),
+                                  ho.data_ptr(), hlse.data_ptr(), hdq.data_ptr(), hdk.data_ptr(),
+                                  hdv.data_ptr(), B, H, N, d, causal, scale, dt_code, hpc,
+                                  e2e_ws.data_ptr(), e2e_ws_bytes, sp)
+            if c:
+                raise fa2.FA2Error("fa2_step_host", c)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -462,7 +470,8 @@ def main():
         e_ms = slowest_rank_ms(a.elapsed_time(b), dist if world > 1 else None, dev)
         e2e = {"value": job_tflops(flops_step, world, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / args.steps}
+               "ms_per_step": e_ms / args.steps, "api": "fa2_step_host",
+               "heads_per_chunk": hpc or -(-(B * H) // 8)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

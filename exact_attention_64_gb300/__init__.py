@@ -25,6 +25,7 @@ __all__ = [
     "forward",
     "forward_instrumented",
     "forward_kv_outer",
+    "step_host",
     "backward",
     "bwd_workspace_size",
     "device_status",
@@ -74,6 +75,9 @@ def load_library() -> ctypes.CDLL:
         "fa2_fwd_split_workspace_size": (sz, [i, i, i, i, i]),
         "fa2_fwd_kv_outer": (i, [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]),
         "fa2_fwd_kv_outer_workspace_size": (sz, [i, i, i, i]),
+        "fa2_step_host": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, sz,
+                              vp]),
+        "fa2_step_host_workspace_size": (sz, [i, i, i, i, i]),
         "fa2_num_splits": (i, [i, i, i, i, i, i]),
         "fa2_bwd_workspace_size": (sz, [i, i, i, i]),
         "fa2_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]),
@@ -121,6 +125,15 @@ def _shape(q: torch.Tensor):
 def _check_tensor(name, t, shape, dtype, device):
     if not t.is_cuda or t.device != device:
         raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name} must have shape {tuple(shape)} and dtype {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_host(name, t, shape, dtype):
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
     if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
         raise ValueError(f"{name} must have shape {tuple(shape)} and dtype {dtype}")
     if not t.is_contiguous():
@@ -215,6 +228,48 @@ def forward_kv_outer(q, k, v, causal: bool = False, scale: float | None = None):
                                 _DTYPES[dt], ws.data_ptr(), nbytes, _stream_ptr(dev))
     _check("fa2_fwd_kv_outer", code)
     return out, lse
+
+
+def step_host(q, k, v, do, causal: bool = False, scale: float | None = None,
+              heads_per_chunk: int = 0, device=None, out=None, workspace=None):
+    """Forward + backward on host (CPU) tensors through fa2_step_host: the
+    copies to and from ``device`` overlap the kernels, chunk by chunk of heads.
+    Inputs should be pinned. Returns host tensors (o, lse, dq, dk, dv); with
+    ``out`` = that 5-tuple of host tensors, writes into them. Synchronises
+    the device's current stream before returning."""
+    B, H, N, d = _shape(q)
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise ValueError("q must be float16 or bfloat16")
+    for name, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+        _check_host(name, t, (B, H, N, d), dt)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        pin = q.is_pinned()
+        o, dq, dk, dv = (torch.empty(q.shape, dtype=dt, pin_memory=pin) for _ in range(4))
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    else:
+        o, lse, dq, dk, dv = out
+    for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_host(name, t, (B, H, N, d), dt)
+    _check_host("lse", lse, (B, H, N), torch.float32)
+    lib = load_library()
+    nbytes = lib.fa2_step_host_workspace_size(B, H, N, d, int(heads_per_chunk))
+    if nbytes == 0:
+        raise FA2Error("fa2_step_host_workspace_size", 1)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    with torch.cuda.device(dev):
+        code = lib.fa2_step_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(),
+                                 o.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                 _DTYPES[dt], int(heads_per_chunk), workspace.data_ptr(),
+                                 workspace.numel(), _stream_ptr(dev))
+        _check("fa2_step_host", code)
+        torch.cuda.current_stream(dev).synchronize()
+    return o, lse, dq, dk, dv
 
 
 def forward_instrumented(q, k, v, causal=False, scale=None):

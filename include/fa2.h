@@ -118,6 +118,36 @@ int fa2_fwd_kv_outer(const void* q, const void* k, const void* v, void* o, float
  * l_i), each array rounded up to 256 bytes. Returns 0 for invalid sizes. */
 size_t fa2_fwd_kv_outer_workspace_size(int B, int H, int N, int d);
 
+/* One forward + backward step on HOST buffers: q, k, v, dO are read from host
+ * memory and o, lse, dq, dk, dv written back to host memory, the copies
+ * overlapped with the kernels. Every (batch, head) is independent
+ * ("FlashAttention学习笔记(2)", V2中的thread blocks排布), so the B*H heads are
+ * cut into chunks of heads_per_chunk consecutive heads and pipelined on three
+ * internal streams: upload of chunk c+1, fa2_fwd + fa2_bwd of chunk c,
+ * download of chunk c-1, with two device slots. The results are the bits of
+ * fa2_fwd + fa2_bwd on device copies of the same tensors.
+ *   q, k, v, dO       : host, [B][H][N][d] dtype, read only. Pinned
+ *                       (page-locked) memory lets the copies overlap.
+ *   o, dq, dk, dv     : host, [B][H][N][d] dtype, written.
+ *   lse               : host, [B][H][N] fp32, written.
+ *   heads_per_chunk   : >= 1, or 0 for ceil(B*H / 8).
+ *   workspace         : device, >= fa2_step_host_workspace_size(...) bytes,
+ *                       256-byte aligned, owned by the caller.
+ *   stream            : the chain starts after the work queued on it and the
+ *                       stream waits for the chain's end; host buffers must
+ *                       stay valid until then.
+ *   other arguments as in fa2_fwd. */
+int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, void* o, float* lse,
+                  void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
+                  int dtype, int heads_per_chunk, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/* Device workspace fa2_step_host needs: two slots of 8 [hc][N][d] 16-bit
+ * tensors and one [hc][N] fp32 tensor, plus fa2_bwd's workspace for one chunk
+ * (hc = heads per chunk as above); each array rounded up to 256 bytes.
+ * Returns 0 for invalid sizes. */
+size_t fa2_step_host_workspace_size(int B, int H, int N, int d, int heads_per_chunk);
+
 /* Bytes of workspace fa2_fwd_split needs: num_splits x B*H x N x (d + 1) fp32
  * (the parts' O / l and logsumexp) plus B*H x ceil(N / 256) x 2 int32 arrival
  * counters, each of the three arrays rounded up to 256 bytes. Returns 0 for

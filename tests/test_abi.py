@@ -123,3 +123,30 @@ def test_kv_outer_rejects_bad_arguments(fa2_lib):
     assert call(base[:5] + [base[5] + 16]) == 3   # workspace must be 256-byte aligned
     assert call(base[:3] + [base[0]] + base[4:]) == 8  # o aliases q
     assert call(base[:5] + [base[1]]) == 8             # workspace overlaps k
+
+
+def test_step_host_rejects_bad_arguments(fa2_lib):
+    lib = fa2_lib.load_library()
+    ws = lib.fa2_step_host_workspace_size(1, 2, 128, 64, 1)
+    assert ws > 0
+    base = [A + i * STEP for i in range(10)]
+
+    def call(ptrs=base, wsz=ws, d=64, hpc=1, causal=0, dtype=1):
+        p = list(ptrs)
+        return lib.fa2_step_host(p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7], p[8], 1, 2, 128, d,
+                                 causal, 0.125, dtype, hpc, p[9], wsz, None)
+
+    assert call([0] + base[1:]) == 1
+    assert call(causal=2) == 1
+    assert call(dtype=7) == 1
+    assert call(hpc=-1) == 1
+    assert call(hpc=3) == 1               # more heads per chunk than heads
+    assert call(d=96) == 2
+    assert call(wsz=ws - 1) == 7
+    assert call(base[:9] + [0]) == 7
+    assert call(base[:9] + [base[9] + 16]) == 3
+    assert lib.fa2_step_host_workspace_size(1, 2, 128, 96, 1) == 0
+    assert lib.fa2_step_host_workspace_size(1, 2, 128, 64, 3) == 0
+    # auto chunking: ceil(B*H / 8) heads per chunk
+    assert lib.fa2_step_host_workspace_size(4, 32, 1024, 128, 0) == \
+        lib.fa2_step_host_workspace_size(4, 32, 1024, 128, 16)
