@@ -8,6 +8,8 @@
 //   copy stream 1 : host -> device  of chunk c+1 (q, k, v, dO)
 //   compute stream: fa2_fwd + fa2_bwd of chunk c
 //   copy stream 2 : device -> host  of chunk c-1 (o, lse, dq, dk, dv)
+// The first and last chunks are a quarter of the others, since their upload
+// and download are not overlapped with anything.
 // Two device slots hold a chunk's inputs and outputs; a slot is refilled only
 // after the compute and the download of the chunk that used it two chunks
 // earlier (event waits). The chain starts after the work already queued on the
@@ -139,9 +141,17 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.up, p.start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.cmp, p.start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.down, p.start, 0);
+  // Chunk sizes: the first upload and the last download are not overlapped
+  // with anything, so the first and last chunks are a quarter of the others.
+  const int small = hc / 4 > 1 ? hc / 4 : 1;
+  auto next_chunk = [&](int rem, bool first) {
+    if (first && rem > small) return small;
+    if (rem > hc + small) return hc;
+    return rem > small ? rem - small : rem;  // <= hc, then the last small chunk
+  };
   int st = FA2_OK;
-  for (int h0 = 0, c = 0; h0 < BH && e == cudaSuccess && st == FA2_OK; h0 += hc, ++c) {
-    const int n = BH - h0 < hc ? BH - h0 : hc;
+  for (int h0 = 0, c = 0, n = 0; h0 < BH && e == cudaSuccess && st == FA2_OK; h0 += n, ++c) {
+    n = next_chunk(BH - h0, c == 0);
     const int s = c % kSlots;
     char* slot = ws + s * L.slot;
     char* din[4] = {slot, slot + L.t16, slot + 2 * L.t16, slot + 3 * L.t16};          // q k v dO
