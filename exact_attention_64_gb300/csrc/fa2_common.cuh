@@ -68,14 +68,6 @@ __host__ __device__ inline int fwd_block_tiles(int m, int N, int N_k, int causal
   return fwd_kv_tile_end(r0, min(N, r0 + kFwdRowsPerCta), N_k, causal);
 }
 
-// CTAs of a split launch: sum over row blocks of their part counts, times B*H.
-inline long long fwd_split_ctas(int N, int N_k, int causal, int num_splits, int n_max, int BH) {
-  long long total = 0;
-  const int M = fwd_num_m_blocks(N);
-  for (int m = 0; m < M; ++m) total += fwd_num_parts(fwd_block_tiles(m, N, N_k, causal), num_splits, n_max);
-  return total * BH;
-}
-
 // The split count: for each candidate s in [1, min(max_splits, num_sms,
 // num_n_blocks)], the SM utilisation is w / ceil(w) with w = workers * s /
 // num_sms waves (the filled fraction of the waves; the page does not define
@@ -177,6 +169,103 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <int N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// Split-mode building blocks shared by the forward and backward kernels.
+// ---------------------------------------------------------------------------
+
+// CTA `cta` of a split launch -> (block, batch*head, part, parts). Blocks are
+// ranked longest first by rank_info(k, &block, &tiles); rank k owns
+// parts(tiles) * BH consecutive CTAs, heads varying fastest. One whole warp
+// scans 32 ranks at a time (inclusive prefix sum of the CTA counts); lane 0 of
+// the hit writes out[0..3]. Past the last part: all zero (no work).
+template <class RankInfo>
+__device__ __forceinline__ void split_locate(int cta, int M, int S, int n_max, int BH, int lane,
+                                             RankInfo rank_info, int* out) {
+  int base = 0;
+  for (int k0 = 0; k0 < M; k0 += 32) {
+    const int k = k0 + lane;
+    int blk = 0, p = 0;
+    if (k < M) {
+      int tiles = 0;
+      rank_info(k, &blk, &tiles);
+      p = fwd_num_parts(tiles, S, n_max);
+    }
+    const int c = p * BH;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, k < M && cta < base + incl);
+    if (hit != 0u) {
+      if (lane == __ffs(hit) - 1) {
+        const int r = cta - (base + incl - c);
+        out[0] = blk;
+        out[1] = r % BH;
+        out[2] = r / BH;
+        out[3] = p;
+      }
+      return;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) out[0] = out[1] = out[2] = out[3] = 0;
+}
+
+// CTAs of a split launch: sum over the ranks of their part counts, times BH.
+template <class TilesOf>
+inline long long split_ctas(int M, int S, int n_max, int BH, TilesOf tiles_of) {
+  long long total = 0;
+  for (int k = 0; k < M; ++k) total += fwd_num_parts(tiles_of(k), S, n_max);
+  return total * BH;
+}
+
+// One warp's 32 TMEM lanes (rows) x D fp32 columns, times `mul` (per lane),
+// to rows [0, rows_valid) of a row-major fp32 matrix starting at dst. Each 32-
+// column block passes through the warp's 4 KiB shared slice (16-byte chunks
+// XOR-swizzled by row) so that every global store is a whole 128-byte row
+// segment. Warp-collective: the whole warp calls it.
+template <int D>
+__device__ __forceinline__ void tmem_rows_to_f32(uint32_t t_src, float mul, float* dst,
+                                                 int rows_valid, int lane, float4* slice) {
+  const int sub = lane >> 3, seg = lane & 7;
+#pragma unroll 1
+  for (int c = 0; c < D; c += 32) {
+    uint32_t x[32];
+    tmem_ld_32x32b_x32(t_src + c, x);
+    tmem_wait_ld();
+    reg_fence(x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      slice[lane * 8 + (k ^ (lane & 7))] =
+          make_float4(__uint_as_float(x[4 * k]) * mul, __uint_as_float(x[4 * k + 1]) * mul,
+                      __uint_as_float(x[4 * k + 2]) * mul, __uint_as_float(x[4 * k + 3]) * mul);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = 4 * i + sub;
+      const float4 val = slice[rr * 8 + (seg ^ (rr & 7))];
+      if (rr < rows_valid) reinterpret_cast<float4*>(dst + static_cast<size_t>(rr) * D + c)[seg] = val;
+    }
+    __syncwarp();
+  }
+}
+
+// Arrival of a 128-thread group on a part counter: every thread's stores are
+// made visible device-wide first, one thread adds 1, and the group learns
+// whether its add completed the count (the group that then merges). Nobody
+// waits on another CTA. Every thread of the group must call it.
+__device__ __forceinline__ bool arrive_last(int* counter, int parts, int bar_id, int* flag) {
+  __threadfence();
+  named_bar_sync(bar_id, 128);
+  if ((threadIdx.x & 127) == 0) *flag = atomicAdd(counter, 1) == parts - 1;
+  named_bar_sync(bar_id, 128);
+  const bool last = *flag != 0;
+  if (last) __threadfence();
+  return last;
 }
 
 }  // namespace fa2

@@ -67,44 +67,6 @@ struct FwdShared {
   int merge[2];  // split mode: this CTA's row tile t arrived last and merges it
 };
 
-// Split mode: CTA `cta` of the 1-D grid -> (row block, batch*head, part, parts).
-// Row blocks are ranked longest first; rank k owns parts(k) * BH consecutive
-// CTAs, heads varying fastest, so that the long parts of every head start
-// before any short one. One warp scans 32 ranks at a time (inclusive prefix
-// sum of the CTA counts) and lane 0 of the hit writes the result.
-__device__ __forceinline__ void fwd_split_locate(int cta, int M, int N, int Nk, int causal, int S,
-                                                 int n_max, int BH, int lane, int* out) {
-  int base = 0;
-  for (int k0 = 0; k0 < M; k0 += 32) {
-    const int k = k0 + lane;
-    int m = 0, p = 0;
-    if (k < M) {
-      m = fwd_m_block_of(k, M, causal);
-      p = fwd_num_parts(fwd_block_tiles(m, N, Nk, causal), S, n_max);
-    }
-    const int c = p * BH;
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, k < M && cta < base + incl);
-    if (hit != 0u) {
-      if (lane == __ffs(hit) - 1) {
-        const int r = cta - (base + incl - c);
-        out[0] = m;
-        out[1] = r % BH;
-        out[2] = r / BH;
-        out[3] = p;
-      }
-      return;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) out[0] = out[1] = out[2] = out[3] = 0;  // past the last part: no work
-}
-
 // Merge of a row tile's K/V parts, run by the warpgroup whose part arrived
 // last ("大猿搬砖简记", thread-block section: the partial results of the
 // blocks that share a worker's K/V range are combined to recover the global
@@ -255,9 +217,14 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(&sh.tmem_base, C::TMEM_COLS);
     tmem_relinquish();
   }
+  // Split mode: one warp places this CTA (row blocks ranked longest first).
   if (S > 1 && warp == 2)
-    fwd_split_locate(blockIdx.x, a.num_m_blocks, N, Nk, CAUSAL, S, a.kv_tiles_max, a.B * a.H, lane,
-                     sh.work);
+    split_locate(blockIdx.x, a.num_m_blocks, S, a.kv_tiles_max, a.B * a.H, lane,
+                 [&](int k, int* blk, int* tiles) {
+                   *blk = fwd_m_block_of(k, a.num_m_blocks, CAUSAL);
+                   *tiles = fwd_block_tiles(*blk, N, Nk, CAUSAL);
+                 },
+                 sh.work);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -490,11 +457,9 @@ __global__ void __launch_bounds__(384, 1)
       // past them) contributes O = 0 with logsumexp -inf. A block with a single
       // part takes the plain epilogue below and writes O and L itself. The TMEM
       // loads are warp-collective: the whole warp runs them, and only the
-      // stores are limited to rows inside the sequence.
-      // Global stores are made whole 128-byte row segments: each warp passes
-      // its 32 rows x 32 columns through a private 4 KiB slice of Q_t's shared
-      // buffer (free once Q_t's last product has completed), 16-byte chunks
-      // XOR-swizzled by row so that neither side conflicts on banks.
+      // stores are limited to rows inside the sequence. Each warp stages its
+      // rows through a private 4 KiB slice of Q_t's buffer, free once Q_t's
+      // last product has completed.
       const bool row_in = my_row < N;
       const size_t part_base =
           (static_cast<size_t>(split) * (static_cast<size_t>(a.B) * a.H) + bh) * static_cast<size_t>(N);
@@ -503,29 +468,8 @@ __global__ void __launch_bounds__(384, 1)
       if (ok && nt > 0) {
         __syncwarp();
         tc_fence_after();
-        const float inv_l = 1.f / l;
-        float4* slice = reinterpret_cast<float4*>(smem + C::OFF_Q + t * C::TILE_BYTES + quad * 4096);
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(t_o + c, o);
-          tmem_wait_ld();
-          reg_fence(o);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            slice[lane * 8 + (k ^ (lane & 7))] =
-                make_float4(__uint_as_float(o[4 * k]) * inv_l, __uint_as_float(o[4 * k + 1]) * inv_l,
-                            __uint_as_float(o[4 * k + 2]) * inv_l, __uint_as_float(o[4 * k + 3]) * inv_l);
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = 4 * i + sub;
-            const float4 val = slice[rr * 8 + (seg ^ (rr & 7))];
-            if (wrow0 + rr < N)
-              reinterpret_cast<float4*>(a.o_part + (part_base + wrow0 + rr) * D + c)[seg] = val;
-          }
-          __syncwarp();
-        }
+        tmem_rows_to_f32<D>(t_o, 1.f / l, a.o_part + (part_base + wrow0) * D, N - wrow0, lane,
+                            reinterpret_cast<float4*>(smem + C::OFF_Q + t * C::TILE_BYTES + quad * 4096));
         if (row_in) a.lse_part[part_base + my_row] = (m_ref * sl2 + lg2_approx(l)) * kLn2;
       } else if (ok) {
         const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -540,23 +484,15 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (row_in) a.lse_part[part_base + my_row] = -INFINITY;
       }
-      // Arrival on the row tile's part counter: every thread's stores are made
-      // visible device-wide first; the group whose arrival completes the
-      // count merges the parts. Nothing waits on another CTA. Every warp of
-      // the group reaches both barriers on every path, aborted or not.
-      __threadfence();
-      named_bar_sync(1 + t, 128);
-      if ((threadIdx.x & 127) == 0) {
-        const size_t ci = (static_cast<size_t>(bh) * a.num_m_blocks + mb) * 2 + t;
-        sh.merge[t] = atomicAdd(a.part_done + ci, 1) == parts - 1;
-      }
-      named_bar_sync(1 + t, 128);
-      if (sh.merge[t]) {
+      // Arrival on the row tile's part counter; the group whose arrival
+      // completes the count merges the parts. Every warp of the group gets
+      // here on every path, aborted or not.
+      const size_t ci = (static_cast<size_t>(bh) * a.num_m_blocks + mb) * 2 + t;
+      if (arrive_last(a.part_done + ci, parts, 1 + t, &sh.merge[t])) {
         // The merge stages its weights in Q_t's buffer. A group with no key in
         // this part skipped every wait, so Q's copy may still be landing there.
         bool q_in = true;
         if (nt == 0 && n_total > 0) q_in = mbar_wait_warp(&sh.q_full, 0, wc);
-        __threadfence();
         if (q_in)
           fwd_merge_rows<D, BF16>(a, bh, wrow0, parts, lane,
                                   reinterpret_cast<float*>(smem + C::OFF_Q + t * C::TILE_BYTES + quad * 4096));
@@ -623,7 +559,9 @@ static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, co
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_m_blocks, a.B, a.H);
   if (a.num_splits > 1) {
-    const long long ctas = fwd_split_ctas(a.N, a.Nk, CAUSAL, a.num_splits, a.kv_tiles_max, a.B * a.H);
+    const long long ctas = split_ctas(a.num_m_blocks, a.num_splits, a.kv_tiles_max, a.B * a.H, [&](int k) {
+      return fwd_block_tiles(fwd_m_block_of(k, a.num_m_blocks, CAUSAL), a.N, a.Nk, CAUSAL);
+    });
     if (ctas < 1 || ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     grid = dim3(static_cast<unsigned>(ctas), 1, 1);
   }
