@@ -56,6 +56,9 @@ _W = [
 # Same per-head shape as the headline with fewer heads: a profiling case whose
 # inputs still exceed L2 but whose captures stay small.
 _W.append(Workload("causal_bf16_b2h16_n8192_d128_qstd3", 2, 16, 8192, 128, "bf16", True, 3.0))
+# The other head size and the other 16-bit type at the long-sequence shape.
+_W.append(Workload("causal_bf16_b4h64_n8192_d64", 4, 64, 8192, 64, "bf16", True))
+_W.append(Workload("causal_fp16_b4h32_n8192_d128", 4, 32, 8192, 128, "fp16", True))
 WORKLOADS = {w.name: w for w in _W}
 
 # Long-sequence, d=128 causal workload the throughput target is stated on.
