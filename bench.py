@@ -206,23 +206,13 @@ TRAFFIC_FILES = {
 }
 
 
-def record_traffic(rep: str, measured) -> None:
-    """profiles/traffic.json from one ncu capture of `measured` (one launch per
-    kernel): DRAM bytes read + written per launch, scaled to the headline
-    workload by the heads processed (same sequence length: each kernel reads its
-    inputs once and writes its outputs once, so traffic grows with B*H), with
-    the hash of the kernel's sources at the time of the capture."""
+def parse_ncu_dram(text: str) -> dict:
+    """{kernel base name: (DRAM bytes read, DRAM bytes written)} of the first
+    launch of each kernel in an `ncu --page raw --csv` export (a header row, a
+    units row, then one row per launch)."""
     import csv
     import io
 
-    from exact_attention_64_gb300.workloads import HEADLINE, WORKLOADS
-
-    head = WORKLOADS[HEADLINE]
-    if (measured.N, measured.d, measured.causal) != (head.N, head.d, head.causal):
-        raise SystemExit("the measured workload must share the headline's N, d and mask")
-    factor = (head.B * head.H) / (measured.B * measured.H)
-    text = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], capture_output=True,
-                          text=True, check=True).stdout
     rows = list(csv.reader(io.StringIO(text)))
     hdr, units, data = rows[0], rows[1], rows[2:]
     scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9}
@@ -231,12 +221,32 @@ def record_traffic(rep: str, measured) -> None:
         i = hdr.index(name)
         return float(row[i]) * scale[units[i]]
 
-    kernels = {}
+    out = {}
     for row in data:
-        name = row[hdr.index("Kernel Name")].split("(")[0].split("<")[0].split()[-1]
-        if name not in TRAFFIC_FILES or name in kernels:
+        name = row[hdr.index("Kernel Name")].split("(")[0].split("<")[0].split()[-1].split("::")[-1]
+        if name not in out:
+            out[name] = (col(row, "dram__bytes_read.sum"), col(row, "dram__bytes_write.sum"))
+    return out
+
+
+def record_traffic(rep: str, measured) -> None:
+    """profiles/traffic.json from one ncu capture of `measured` (one launch per
+    kernel): DRAM bytes read + written per launch, scaled to the headline
+    workload by the heads processed (same sequence length: each kernel reads its
+    inputs once and writes its outputs once, so traffic grows with B*H), with
+    the hash of the kernel's sources at the time of the capture."""
+    from exact_attention_64_gb300.workloads import HEADLINE, WORKLOADS
+
+    head = WORKLOADS[HEADLINE]
+    if (measured.N, measured.d, measured.causal) != (head.N, head.d, head.causal):
+        raise SystemExit("the measured workload must share the headline's N, d and mask")
+    factor = (head.B * head.H) / (measured.B * measured.H)
+    text = subprocess.run(["ncu", "-i", rep, "--page", "raw", "--csv"], capture_output=True,
+                          text=True, check=True).stdout
+    kernels = {}
+    for name, (rd, wr) in parse_ncu_dram(text).items():
+        if name not in TRAFFIC_FILES:
             continue
-        rd, wr = col(row, "dram__bytes_read.sum"), col(row, "dram__bytes_write.sum")
         kernels[name] = {
             "workload": head.name,
             "bytes_per_launch": int(round((rd + wr) * factor)),
