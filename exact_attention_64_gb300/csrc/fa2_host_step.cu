@@ -69,7 +69,10 @@ struct Pipe {
 
 constexpr int kMaxDevices = 64;
 Pipe g_pipes[kMaxDevices];
-std::mutex g_pipe_mu;
+// One lock per device: a call holds its device's lock while it enqueues (the
+// events of the device's pipeline are shared by its calls); calls on other
+// devices proceed.
+std::mutex g_pipe_mu[kMaxDevices];
 
 cudaError_t pipe_init(Pipe& p) {
   if (p.ready) return cudaSuccess;
@@ -122,7 +125,7 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA2_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_pipe_mu);
+  std::lock_guard<std::mutex> lock(g_pipe_mu[dev]);
   Pipe& p = g_pipes[dev];
   if (pipe_init(p) != cudaSuccess) return FA2_ERR_CUDA;
 

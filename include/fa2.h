@@ -133,9 +133,11 @@ size_t fa2_fwd_kv_outer_workspace_size(int B, int H, int N, int d);
  *   heads_per_chunk   : >= 1, or 0 for ceil(B*H / 8).
  *   workspace         : device, >= fa2_step_host_workspace_size(...) bytes,
  *                       256-byte aligned, owned by the caller.
- *   stream            : the chain starts after the work queued on it and the
- *                       stream waits for the chain's end; host buffers must
- *                       stay valid until then.
+ *   stream            : a stream of the current device (or NULL). The chain
+ *                       starts after the work queued on it and the stream
+ *                       waits for the chain's end; host buffers must stay
+ *                       valid until then. Calls on one device are enqueued
+ *                       one at a time (a per-device lock).
  *   other arguments as in fa2_fwd. */
 int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, void* o, float* lse,
                   void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal, float scale,
