@@ -399,7 +399,6 @@ def main():
     t_fwd = [a.elapsed_time(b) for a, b in fwd_ev]
     t_pre = [e[0].elapsed_time(e[1]) for e in bwd_ev]
     t_kv = [e[1].elapsed_time(e[2]) for e in bwd_ev]
-    t_dq = [e[2].elapsed_time(e[3]) for e in bwd_ev]
     elapsed_ms = slowest_rank_ms(elapsed_ms, dist if world > 1 else None, dev)
 
     flops_step = w.fwd_flops() + w.bwd_flops()
@@ -407,15 +406,14 @@ def main():
     pk = peaks()
     mean = statistics.mean
     # Algorithmic work per launch. The convention counts the forward as two
-    # N x N x d GEMM units (S, PV) and the backward as five (2.5x): the dK/dV
-    # kernel performs four of them (S^T, dP^T, dV, dK); the dQ kernel performs
-    # the fifth (dQ) plus two recomputations (S, dP) that the convention does
-    # not count, so only one unit is credited to it.
+    # N x N x d GEMM units (S, PV) and the backward as five (2.5x). The
+    # backward's main launch runs the dK/dV workers (S^T, dP^T, dV, dK: four
+    # units) and the dQ workers (dQ, plus the recomputed S and dP that the
+    # convention does not count): five units credited.
     fw = w.fwd_flops()
     kernels = {
         ("fa1_order_fwd_kernel" if kv_outer else "fa2_fwd_kernel"): (mean(t_fwd), fw, "tensor"),
-        "fa2_bwd_dkdv_kernel": (mean(t_kv), 2.0 * fw, "tensor"),
-        "fa2_bwd_dq_kernel": (mean(t_dq), 0.5 * fw, "tensor"),
+        "fa2_bwd_main_kernel": (mean(t_kv), 2.5 * fw, "tensor"),
         "fa2_bwd_pre_kernel": (mean(t_pre), B * H * N * (2 * d * 2 + 4 + 8), "hbm"),
     }
     dom = max(kernels, key=lambda n: kernels[n][0])
@@ -441,7 +439,7 @@ def main():
     tot = sum(x[0] for x in kernels.values())
     per_kernel = {n: {"ms": t, "share": t / tot} for n, (t, _, _) in kernels.items()}
     fwd_tf = fw / (mean(t_fwd) * 1e-3) / 1e12
-    bwd_tf = w.bwd_flops() / ((mean(t_pre) + mean(t_kv) + mean(t_dq)) * 1e-3) / 1e12
+    bwd_tf = w.bwd_flops() / ((mean(t_pre) + mean(t_kv)) * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ----
     e2e = None

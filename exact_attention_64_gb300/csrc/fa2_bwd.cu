@@ -1,17 +1,19 @@
-// FlashAttention-2 backward for sm_103a: three kernels on one stream.
+// FlashAttention-2 backward for sm_103a: two launches on one stream, the
+// preprocessing pass and one main launch that runs the dK/dV workers and the
+// dQ workers (fa2_bwd_main_kernel).
 //
 //  1. fa2_bwd_pre_kernel  D_i = sum_c dO[i][c] * O[i][c] in fp32 from the stored
 //                         O, and L_i * log2(e). The D shortcut stands in for
 //                         rowsum(P o dP) ("大猿搬砖简记", V2 backward, last
 //                         paragraph).
-//  2. fa2_bwd_dkdv_kernel K/V outer, Q inner ("FlashAttention学习笔记(2)",
+//  2. dK/dV workers      K/V outer, Q inner ("FlashAttention学习笔记(2)",
 //                         Foward和backward中的thread block划分; "大猿搬砖简记",
 //                         V2 backward): one CTA per 128-key column block keeps
 //                         K_j, V_j in shared memory and dK_j, dV_j in TMEM while
 //                         128-row query tiles stream past; S and P are
 //                         recomputed from L ("flash-attention123和ring-attention",
 //                         优化1).
-//  3. fa2_bwd_dq_kernel   dQ, which accumulates along the key direction (the
+//  3. dQ workers         dQ, which accumulates along the key direction (the
 //                         "awkward" gradient of the V2 backward), gets a worker
 //                         of its own that owns a 128-row query tile and
 //                         accumulates dQ in fp32 TMEM over the visible K/V
@@ -19,9 +21,9 @@
 //                         variant: no atomics, and dQ is bit-reproducible.
 //
 // Products (tcgen05, 16-bit operands, fp32 accumulate in TMEM):
-//   dK/dV kernel, per query tile i:  S^T = K Q_i^T, dP^T = V dO_i^T   (SS, M=128 keys, N=128 queries)
+//   dK/dV worker, per query tile i:  S^T = K Q_i^T, dP^T = V dO_i^T   (SS, M=128 keys, N=128 queries)
 //                                    dV += P^T dO_i, dK += dS^T Q_i   (TS, A from TMEM, M=128 keys, N=d)
-//   dQ kernel, per K/V tile j:       S = Q K_j^T, dP = dO V_j^T        (SS, M=128 queries, N=128 keys)
+//   dQ worker, per K/V tile j:       S = Q K_j^T, dP = dO V_j^T        (SS, M=128 queries, N=128 keys)
 //                                    dQ += dS K_j                      (TS, A from TMEM, M=128 queries, N=d)
 // with P = exp2(S * scale*log2e - L*log2e) and dS = P o (dP - D).
 #include <cuda_fp16.h>
@@ -290,12 +292,13 @@ __device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r
 // dP^T region after dP^T(i) has been read. The exponentials of P^T(i) thus
 // overlap dV/dK(i-1) and dP^T(i) on the tensor core, and the only chain from
 // one tile to the next is dP^T -> dS^T -> dV, dK -> dP^T.
+// One dK/dV worker (key block nb of batch*head bh), run by a CTA of the
+// backward's main launch.
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
-    fa2_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
-                        const BwdArgs a) {
+__device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                             const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+                                             const CUtensorMap& tm_dk, const CUtensorMap& tm_dv,
+                                             const BwdArgs& a, const int nb, const int bh) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -304,8 +307,6 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;    // queries
   const int Nk = a.Nk;  // keys and values
-  const int nb = blockIdx.x;                     // key block, fastest grid axis
-  const int bh = blockIdx.y * a.H + blockIdx.z;  // grid = (n block, batch, head)
   const int n0 = nb * kTileRows;
   const int i_begin = bwd_q_tile_begin(nb, CAUSAL);
   // 0 when no query sees these keys (causal, more keys than queries): the
@@ -584,11 +585,13 @@ __global__ void __launch_bounds__(384, 1)
 // ---------------------------------------------------------------------------
 // Warp roles: warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 compute dS for key
 // columns [0,64) and [64,128) of each K/V tile (TMEM lane = query row).
+// One dQ worker (query block of longest-first rank `rank`, batch*head bh),
+// run by a CTA of the backward's main launch.
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
-    fa2_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                      const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a, int num_m_blocks) {
+__device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                           const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+                                           const CUtensorMap& tm_dq, const BwdArgs& a,
+                                           const int num_m_blocks, const int rank, const int bh) {
   using C = BwdCfg<D>;
   using Q = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -597,8 +600,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N;
-  const int mb = dq_m_block_of(blockIdx.x, num_m_blocks, CAUSAL);
-  const int bh = blockIdx.y * a.H + blockIdx.z;
+  const int mb = dq_m_block_of(rank, num_m_blocks, CAUSAL);
   const int q0 = mb * kTileRows;
   const int n_kv = fwd_kv_tile_end(q0, min(N, q0 + kTileRows), a.Nk, CAUSAL);
 
@@ -768,6 +770,37 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ---------------------------------------------------------------------------
+// 4. The backward's main launch: the dK/dV workers, then the dQ workers
+// ---------------------------------------------------------------------------
+// The two passes read the same inputs and D, L from the preprocessing pass,
+// and write different outputs, so they share one grid: CTAs [0, kv_ctas) are
+// dK/dV workers in the pages' (key block, batch, head) order (key block
+// fastest, then batch, then head), the rest dQ workers in the same order over
+// the longest-first query-block ranks. CTAs start in index order, so dQ
+// workers take the SMs that short dK/dV workers free while the long ones are
+// still running.
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+    fa2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                        const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a, int num_m_blocks,
+                        int kv_ctas) {
+  const int x = blockIdx.x;
+  if (x < kv_ctas) {
+    const int nkb = bwd_num_n_blocks(a.Nk);
+    const int rest = x / nkb;  // batch + B * head
+    bwd_dkdv_cta<D, BF16, CAUSAL>(tm_q, tm_k, tm_v, tm_do, tm_dk, tm_dv, a, x % nkb,
+                                  (rest % a.B) * a.H + rest / a.B);
+  } else {
+    const int y = x - kv_ctas;
+    const int rest = y / num_m_blocks;
+    bwd_dq_cta<D, BF16, CAUSAL>(tm_q, tm_k, tm_v, tm_do, tm_dq, a, num_m_blocks, y % num_m_blocks,
+                                (rest % a.B) * a.H + rest / a.B);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host-side launcher
 // ---------------------------------------------------------------------------
 static int g_num_sms = 0;
@@ -799,28 +832,22 @@ static cudaError_t launch_bwd_t(const void* o, const void* dO, const float* lse,
   }
   if (ev) cudaEventRecord(ev[1], stream);
   {
-    auto kern = fa2_bwd_dkdv_kernel<D, BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    dim3 grid(bwd_num_n_blocks(a.Nk), a.B, a.H);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
-                                                      maps[5], a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  if (ev) cudaEventRecord(ev[2], stream);
-  {
-    auto kern = fa2_bwd_dq_kernel<D, BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         DqCfg<D>::SMEM_ALLOC);
+    auto kern = fa2_bwd_main_kernel<D, BF16, CAUSAL>;
+    const int smem = C::SMEM_ALLOC > DqCfg<D>::SMEM_ALLOC ? C::SMEM_ALLOC : DqCfg<D>::SMEM_ALLOC;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int nm = dq_num_m_blocks(a.N);
-    dim3 grid(nm, a.B, a.H);
-    kern<<<grid, C::THREADS, DqCfg<D>::SMEM_ALLOC, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[6],
-                                                      a, nm);
+    const long long kv_ctas = static_cast<long long>(bwd_num_n_blocks(a.Nk)) * BH;
+    const long long total = kv_ctas + static_cast<long long>(nm) * BH;
+    if (total > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    kern<<<static_cast<unsigned>(total), C::THREADS, smem, stream>>>(
+        maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], a, nm, static_cast<int>(kv_ctas));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  // The dK/dV and dQ workers share one launch: the third and fourth events
+  // both mark its end.
+  if (ev) cudaEventRecord(ev[2], stream);
   if (ev) cudaEventRecord(ev[3], stream);
   return cudaSuccess;
 }

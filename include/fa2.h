@@ -203,8 +203,8 @@ int fa2_bwd_qk(const void* q, const void* k, const void* v, const void* o, const
 
 /* fa2_bwd, plus: phase_events (4 cudaEvent_t created by the caller, or NULL)
  * are recorded on `stream` before the preprocessing kernel, between it and
- * the dK/dV kernel, between that and the dQ kernel, and after it, so the
- * caller can time each of the three kernels. */
+ * the main launch (the dK/dV and dQ workers), and twice after the main launch,
+ * so the caller can time the two launches. */
 int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, const float* lse,
                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,

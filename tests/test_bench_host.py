@@ -24,16 +24,16 @@ NCU_RAW = "\n".join([
     '"0","void fa2::fa2_fwd_kernel<128, true, true>(CUtensorMap_st, FwdArgs)","201.5","51765.5","411.7"',
     '"1","void fa2::fa2_bwd_pre_kernel<128, true>(const unsigned short *, int)","0.135","4.4","27.3"',
     '"2","void fa2::fa2_fwd_kernel<128, true, true>(CUtensorMap_st, FwdArgs)","999","999","1"',
-    '"3","fa2_bwd_dq_kernel","1.5","2","520"',
+    '"3","fa2_bwd_main_kernel","1.5","2","520"',
 ])
 
 
 def test_ncu_export_parsing(bench):
     got = bench.parse_ncu_dram(NCU_RAW)
-    assert set(got) == {"fa2_fwd_kernel", "fa2_bwd_pre_kernel", "fa2_bwd_dq_kernel"}
+    assert set(got) == {"fa2_fwd_kernel", "fa2_bwd_pre_kernel", "fa2_bwd_main_kernel"}
     assert got["fa2_fwd_kernel"] == pytest.approx((201.5e6, 51765.5e3))  # first launch only
     assert got["fa2_bwd_pre_kernel"] == pytest.approx((0.135e6, 4.4e3))
-    assert got["fa2_bwd_dq_kernel"] == pytest.approx((1.5e6, 2e3))
+    assert got["fa2_bwd_main_kernel"] == pytest.approx((1.5e6, 2e3))
 
 
 def test_clock_summary(bench):
