@@ -200,8 +200,7 @@ def run_reference(args, w, rank, world):
 
 TRAFFIC_FILES = {
     "fa2_fwd_kernel": ["fa2_fwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
-    "fa2_bwd_dkdv_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
-    "fa2_bwd_dq_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_main_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
     "fa2_bwd_pre_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
 }
 
