@@ -503,8 +503,9 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # fwd, bwd pre, dK/dV, dQ per step (a split forward adds a counter memset, not a kernel)
-        "gpu_launches": 4 * args.steps,
+        # forward, backward preprocessing, backward main launch (dK/dV and dQ
+        # workers) per step; a split forward adds a counter memset, not a kernel
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:
