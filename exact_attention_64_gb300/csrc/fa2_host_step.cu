@@ -5,9 +5,10 @@
 // so a step over host-resident tensors can be cut into chunks of consecutive
 // heads -- contiguous slabs of every [B][H][N][d] tensor -- and run as a
 // three-stage pipeline on internal streams:
-//   copy stream 1 : host -> device  of chunk c+1 (q, k, v, dO)
-//   compute stream: fa2_fwd + fa2_bwd of chunk c
-//   copy stream 2 : device -> host  of chunk c-1 (o, lse, dq, dk, dv)
+//   copy stream 1  : host -> device  of chunk c+1 (q, k, v, dO)
+//   compute streams: fa2_fwd + fa2_bwd of chunk c, on the stream of its slot
+//                    (consecutive chunks' kernels may overlap)
+//   copy stream 2  : device -> host  of chunk c-1 (o, lse, dq, dk, dv)
 // The first and last chunks are a quarter of the others, since their upload
 // and download are not overlapped with anything.
 // Two device slots hold a chunk's inputs and outputs; a slot is refilled only
@@ -34,7 +35,7 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 struct ChunkLayout {
   size_t t16;      // bytes of one [hc][N][d] 16-bit tensor, rounded to 256
   size_t lse;      // bytes of one [hc][N] fp32 tensor, rounded to 256
-  size_t slot;     // bytes of one slot: 8 16-bit tensors + lse
+  size_t slot;     // bytes of one slot: 8 16-bit tensors + lse, then fa2_bwd's workspace
   size_t bwd_ws;   // fa2_bwd workspace for one chunk
   size_t total;
 };
@@ -45,10 +46,10 @@ bool layout(int B, int H, int N, int d, int hc, ChunkLayout* L) {
     return false;
   L->t16 = up256(static_cast<size_t>(hc) * N * d * 2);
   L->lse = up256(static_cast<size_t>(hc) * N * 4);
-  L->slot = 8 * L->t16 + L->lse;
   L->bwd_ws = up256(fa2_bwd_workspace_size(1, hc, N, d));
   if (L->bwd_ws == 0) return false;
-  L->total = kSlots * L->slot + L->bwd_ws;
+  L->slot = 8 * L->t16 + L->lse + L->bwd_ws;
+  L->total = kSlots * L->slot;
   return true;
 }
 
@@ -62,8 +63,8 @@ int chunk_heads(int B, int H, int heads_per_chunk) {
 // Internal streams and events of one device, created on first use.
 struct Pipe {
   bool ready = false;
-  cudaStream_t up = nullptr, cmp = nullptr, down = nullptr;
-  cudaEvent_t start = nullptr, done[3] = {};  // done: end of the up, compute, down streams
+  cudaStream_t up = nullptr, cmp[kSlots] = {}, down = nullptr;
+  cudaEvent_t start = nullptr, done[kSlots + 2] = {};  // done: end of every internal stream
   cudaEvent_t uploaded[kSlots] = {}, computed[kSlots] = {}, downloaded[kSlots] = {};
 };
 
@@ -84,10 +85,10 @@ cudaError_t pipe_init(Pipe& p) {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   };
   mk_stream(&p.up);
-  mk_stream(&p.cmp);
+  for (int s = 0; s < kSlots; ++s) mk_stream(&p.cmp[s]);
   mk_stream(&p.down);
   mk_event(&p.start);
-  for (int i = 0; i < 3; ++i) mk_event(&p.done[i]);
+  for (int i = 0; i < kSlots + 2; ++i) mk_event(&p.done[i]);
   for (int s = 0; s < kSlots; ++s) {
     mk_event(&p.uploaded[s]);
     mk_event(&p.computed[s]);
@@ -131,7 +132,6 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
 
   const cudaStream_t caller = static_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  char* bwd_ws = ws + kSlots * L.slot;
   const int BH = B * H;
   const size_t row16 = static_cast<size_t>(N) * d * 2;  // one head of a 16-bit tensor
   const size_t row32 = static_cast<size_t>(N) * 4;      // one head of lse
@@ -142,7 +142,7 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
 
   cudaError_t e = cudaEventRecord(p.start, caller);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.up, p.start, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(p.cmp, p.start, 0);
+  for (int i = 0; i < kSlots && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(p.cmp[i], p.start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(p.down, p.start, 0);
   // Chunk sizes: the first upload and the last download are not overlapped
   // with anything, so the first and last chunks are a quarter of the others.
@@ -160,6 +160,10 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
     char* din[4] = {slot, slot + L.t16, slot + 2 * L.t16, slot + 3 * L.t16};          // q k v dO
     char* dout[4] = {slot + 4 * L.t16, slot + 5 * L.t16, slot + 6 * L.t16, slot + 7 * L.t16};  // o dq dk dv
     float* dlse = reinterpret_cast<float*>(slot + 8 * L.t16);
+    char* bwd_ws = slot + 8 * L.t16 + L.lse;
+    // Chunk c computes on the stream of its slot, so consecutive chunks'
+    // kernels may overlap and fill each other's tails.
+    const cudaStream_t cmp = p.cmp[s];
     const size_t off16 = static_cast<size_t>(h0) * row16, bytes16 = static_cast<size_t>(n) * row16;
     // Upload: the slot's inputs are free once the compute of chunk c - 2 is done.
     if (c >= kSlots) e = cudaStreamWaitEvent(p.up, p.computed[s], 0);
@@ -168,15 +172,15 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
     if (e == cudaSuccess) e = cudaEventRecord(p.uploaded[s], p.up);
     // Compute: after the upload, and after the download of chunk c - 2 has read
     // the slot's outputs.
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(p.cmp, p.uploaded[s], 0);
-    if (e == cudaSuccess && c >= kSlots) e = cudaStreamWaitEvent(p.cmp, p.downloaded[s], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cmp, p.uploaded[s], 0);
+    if (e == cudaSuccess && c >= kSlots) e = cudaStreamWaitEvent(cmp, p.downloaded[s], 0);
     if (e != cudaSuccess) break;
-    st = fa2_fwd(din[0], din[1], din[2], dout[0], dlse, 1, n, N, d, causal, scale, dtype, p.cmp);
+    st = fa2_fwd(din[0], din[1], din[2], dout[0], dlse, 1, n, N, d, causal, scale, dtype, cmp);
     if (st == FA2_OK)
       st = fa2_bwd(din[0], din[1], din[2], dout[0], dlse, din[3], dout[1], dout[2], dout[3], 1, n, N,
-                   d, causal, scale, dtype, bwd_ws, L.bwd_ws, p.cmp);
+                   d, causal, scale, dtype, bwd_ws, L.bwd_ws, cmp);
     if (st != FA2_OK) break;
-    e = cudaEventRecord(p.computed[s], p.cmp);
+    e = cudaEventRecord(p.computed[s], cmp);
     // Download.
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p.down, p.computed[s], 0);
     for (int t = 0; t < 4 && e == cudaSuccess; ++t)
@@ -189,9 +193,12 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
   // Join: the caller's stream continues after everything queued on the three
   // internal streams, on the error paths too, so that nothing queued here
   // outlives what the caller waits for.
-  const cudaStream_t internal[3] = {p.up, p.cmp, p.down};
+  cudaStream_t internal[kSlots + 2];
+  internal[0] = p.up;
+  internal[1] = p.down;
+  for (int i = 0; i < kSlots; ++i) internal[2 + i] = p.cmp[i];
   cudaError_t ej = cudaSuccess;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < kSlots + 2; ++i) {
     const cudaError_t a = cudaEventRecord(p.done[i], internal[i]);
     const cudaError_t b = a == cudaSuccess ? cudaStreamWaitEvent(caller, p.done[i], 0) : a;
     if (ej == cudaSuccess) ej = b;

@@ -144,9 +144,9 @@ int fa2_step_host(const void* q, const void* k, const void* v, const void* dO, v
                   int dtype, int heads_per_chunk, void* workspace, size_t workspace_bytes,
                   void* stream);
 
-/* Device workspace fa2_step_host needs: two slots of 8 [hc][N][d] 16-bit
- * tensors and one [hc][N] fp32 tensor, plus fa2_bwd's workspace for one chunk
- * (hc = heads per chunk as above); each array rounded up to 256 bytes.
+/* Device workspace fa2_step_host needs: two slots, each of 8 [hc][N][d]
+ * 16-bit tensors, one [hc][N] fp32 tensor and fa2_bwd's workspace for one
+ * chunk (hc = heads per chunk as above); each array rounded up to 256 bytes.
  * Returns 0 for invalid sizes. */
 size_t fa2_step_host_workspace_size(int B, int H, int N, int d, int heads_per_chunk);
 
