@@ -2,8 +2,8 @@
 """Throughput of one FlashAttention-2 training step (forward + backward) on GB300.
 
 A step is one pass of the whole hot path over one batch of synthetic input:
-fa2_fwd (O, L) then fa2_bwd (D preprocessing, the K/V-outer dK/dV kernel, the
-Q-outer dQ kernel). The metric is TFLOP/s with the usual FLOP convention
+fa2_fwd (O, L) then fa2_bwd (D preprocessing, then one launch of the K/V-outer dK/dV workers and the
+Q-outer dQ workers). The metric is TFLOP/s with the usual FLOP convention
 (forward 4*B*H*N^2*d, halved under the causal mask; backward 2.5x forward).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fa2|reference]

@@ -43,7 +43,7 @@ struct BwdCfg {
   static constexpr int OFF_FIX1 = TILE_BYTES;
   static constexpr int OFF_STR0 = 2 * TILE_BYTES;       // streamed pair, NS stages each
   static constexpr int OFF_STR1 = OFF_STR0 + NS * TILE_BYTES;
-  // dK/dV kernel: per-warp copies of L*log2e and D for its 64 query columns
+  // dK/dV workers: per-warp copies of L*log2e and D for its 64 query columns
   // (8 warps x 128 floats), read as shared-memory broadcasts.
   static constexpr int OFF_LD = OFF_STR1 + NS * TILE_BYTES;
   static constexpr int SMEM_BYTES = OFF_LD + 8 * 128 * 4;
@@ -51,12 +51,12 @@ struct BwdCfg {
   static constexpr int SMEM_ALLOC = (SMEM_BYTES + 1024 > 118784) ? SMEM_BYTES + 1024 : 118784;
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
-  // dK/dV kernel TMEM: dV, dK accumulators, S^T and dP^T. A warpgroup owns 64
+  // dK/dV worker TMEM: dV, dK accumulators, S^T and dP^T. A warpgroup owns 64
   // query columns of each region; once it has read dP^T for 32 of its queries
   // (half h), it writes those 32 columns back as 16 columns of P^T and 16 of
   // dS^T (16-bit pairs): [P^T h0 | dS^T h0 | P^T h1 | dS^T h1].
   static constexpr uint32_t KV_DV = 0, KV_DK = D, KV_ST = 2 * D, KV_DPT = 2 * D + 128;
-  // dQ kernel TMEM: S, dP, the dQ accumulator and two dS buffers.
+  // dQ worker TMEM: S, dP, the dQ accumulator and two dS buffers.
   static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256;
   __host__ __device__ static constexpr uint32_t Q_DS(int b) { return 256 + D + 64 * b; }
 };
@@ -74,7 +74,7 @@ struct BwdKvShared {
   int abort_flag;
 };
 
-// dQ kernel shared-memory plan: Q, dO resident; K_j in a 3-deep ring (it is
+// dQ worker shared-memory plan: Q, dO resident; K_j in a 3-deep ring (it is
 // read by S(j) and, last, by dQ(j)); V_j in a 2-deep ring (read only by
 // dP(j), so it is freed early). 224 KiB at d = 128.
 template <int D>
@@ -210,7 +210,7 @@ __device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uin
   }
 }
 
-// P^T for 32 query columns q_first.. of key row kg (dK/dV kernel):
+// P^T for 32 query columns q_first.. of key row kg (dK/dV workers):
 // p[c] = exp2(S^T[c] * scale*log2e + nl_cols[c]), nl_cols = -(L*log2e) in registers. With MASK, pairs outside the
 // sequence or with key > query (causal) get 0. MASK is a template parameter so
 // that tiles off the diagonal run a loop with no per-element branches, which
@@ -233,7 +233,7 @@ __device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const floa
   }
 }
 
-// dS for 64 key columns of query row my_row (dQ kernel), packed to 16-bit
+// dS for 64 key columns of query row my_row (dQ workers), packed to 16-bit
 // pairs: dS = P o (dP - D) with P = exp2(S * scale*log2e - L*log2e). With MASK,
 // keys at or past lim and rows past the sequence get P = 0. Column pairs use
 // packed fp32 (f32x2) arithmetic.
@@ -282,7 +282,7 @@ __device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r
 }
 
 // ---------------------------------------------------------------------------
-// 2. dK / dV kernel (K/V outer, Q inner)
+// 2. dK / dV workers (K/V outer, Q inner)
 // ---------------------------------------------------------------------------
 // Warp roles: warp 0 TMA; warp 1 issues the score products S^T(i), dP^T(i);
 // warp 2 issues the gradient products dV(i), dK(i); warps 4-7 and 8-11 compute
@@ -581,7 +581,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
 }
 
 // ---------------------------------------------------------------------------
-// 3. dQ kernel (Q outer, K/V inner)
+// 3. dQ workers (Q outer, K/V inner)
 // ---------------------------------------------------------------------------
 // Warp roles: warp 0 TMA, warp 1 MMA, warps 4-7 and 8-11 compute dS for key
 // columns [0,64) and [64,128) of each K/V tile (TMEM lane = query row).
