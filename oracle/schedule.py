@@ -18,11 +18,20 @@ paragraph): when the (row block, batch, head) workers cannot fill the SMs, the
 K/V range of each worker may be cut into num_splits parts whose partial results
 are merged afterwards. The split count is chosen by computing the SM
 utilisation of each candidate, taking the best, and picking the smallest
-candidate whose utilisation is at least 0.95 of it. The page does not define
-the utilisation; reading: with w = workers * s / num_sms waves, utilisation is
-w / ceil(w), the filled fraction of the waves launched. Candidates run from 1
-to min(max_splits, num_sms, number of K/V tiles): more parts than K/V tiles
-leave parts empty, more than the SM count add no wave.
+candidate whose utilisation is at least 0.95 of it. Candidates run from 1 to
+min(max_splits, num_sms, number of K/V tiles): more parts than K/V tiles leave
+parts empty, more than the SM count add no wave. The page does not define the
+utilisation. Two readings are kept here:
+  * split_utilisation: the filled fraction of the waves, w / ceil(w) with
+    w = workers * s / num_sms, which counts CTAs and treats them as equal;
+  * split_utilisation_makespan (the library's rule): the fraction of the SMs'
+    time spent on K/V tiles, useful tiles / (num_sms * makespan), when the
+    launch's CTAs start in launch order, each on the SM that frees first, and
+    a CTA takes its tiles plus a fixed cost, plus a further cost if its row
+    block is split (its partial write and its share of the merge). Under the
+    causal mask the workers are unequal and the waves reading cannot see the
+    tail; this one can, and with equal workers and no costs it reduces to the
+    waves reading.
 
 Causal tile skipping ("flash-attention123和ring-attention", 优化3): key/query
 tile pairs that the causal mask hides completely are dropped, not computed.
@@ -32,6 +41,8 @@ masked iff every key index in it exceeds every query index in it.
 """
 
 from __future__ import annotations
+
+import heapq
 
 __all__ = [
     "ceil_div",
@@ -44,6 +55,12 @@ __all__ = [
     "num_splits_heuristic",
     "split_num_parts",
     "split_part_range",
+    "split_launch",
+    "greedy_makespan",
+    "split_utilisation_makespan",
+    "num_splits_makespan",
+    "SPLIT_CTA_COST",
+    "SPLIT_PART_COST",
 ]
 
 
@@ -152,3 +169,62 @@ def split_part_range(j_begin: int, j_end: int, parts: int, part: int):
     [j_begin, j_end): lengths floor or ceil of len / parts, in order."""
     n = j_end - j_begin
     return (j_begin + part * n // parts, j_begin + (part + 1) * n // parts)
+
+
+# Costs of the makespan reading, in K/V tiles of work (one tile = one 128-key
+# step of a 256-row forward worker). Fitted to forward times measured on
+# GB300 over split counts 1..16 of six long-sequence shapes (d = 128, causal
+# and not): a CTA's fixed start and finish costs about one tile, and a part of
+# a split row block about six more (its fp32 partial write and merge share).
+SPLIT_CTA_COST = 1
+SPLIT_PART_COST = 6
+
+
+def split_launch(block_tiles, BH: int, s: int):
+    """The CTAs of a forward launch with split count s, in launch order: the
+    row blocks in the given order (longest first), each block's parts in
+    order, each part repeated for the BH heads (heads fastest). Returns a list
+    of (tiles, split) pairs, split being True when the block has more than one
+    part (s = 1: one part per block)."""
+    n_max = max(block_tiles)
+    out = []
+    for n in block_tiles:
+        p = split_num_parts(n, s, n_max)
+        for part in range(p):
+            lo, hi = split_part_range(0, n, p, part)
+            out.extend([(hi - lo, p > 1)] * BH)
+    return out
+
+
+def greedy_makespan(costs, num_sms: int):
+    """Time at which the last SM finishes when every CTA, in launch order,
+    starts on the SM that becomes free first (list scheduling; the SMs' free
+    times kept in a heap)."""
+    free = [0] * num_sms
+    for c in costs:
+        heapq.heappush(free, heapq.heappop(free) + c)
+    return max(free)
+
+
+def split_utilisation_makespan(block_tiles, BH: int, num_sms: int, s: int,
+                               cta_cost=SPLIT_CTA_COST, part_cost=SPLIT_PART_COST) -> float:
+    """Useful tiles / (num_sms * makespan) of the split-s launch."""
+    ctas = split_launch(block_tiles, BH, s)
+    useful = sum(t for t, _ in ctas)
+    span = greedy_makespan([t + cta_cost + (part_cost if sp else 0) for t, sp in ctas], num_sms)
+    return useful / (num_sms * span)
+
+
+def num_splits_makespan(block_tiles, BH: int, num_sms: int, max_splits: int,
+                        cta_cost=SPLIT_CTA_COST, part_cost=SPLIT_PART_COST) -> int:
+    """The page's selection rule over the makespan utilisation: the best over
+    the candidates 1 .. min(max_splits, num_sms, K/V tiles of the longest
+    block), then the smallest candidate within 0.95 of it."""
+    top = max(1, min(max_splits, num_sms, max(block_tiles)))
+    eff = [split_utilisation_makespan(block_tiles, BH, num_sms, c, cta_cost, part_cost)
+           for c in range(1, top + 1)]
+    best = max(eff)
+    for c in range(1, top + 1):
+        if eff[c - 1] >= 0.95 * best:
+            return c
+    return 1

@@ -28,6 +28,23 @@ def test_num_m_block_is_ceil():
         assert schedule.fwd_grid(1, 1, N, bm)[0] == want
 
 
+def test_bwd_grid_worked_by_hand():
+    """One backward worker per 128-key column block: ceil(N / 128) blocks, so
+    N = 1 and N = 128 give one block, N = 129 two, N = 16384 exactly 128 (a
+    floor division would give 0, 1, 1 and 128), with (batch, heads) after it."""
+    for (B, H, N), want in (((1, 1, 1), (1, 1, 1)), ((2, 3, 128), (1, 2, 3)),
+                            ((1, 1, 129), (2, 1, 1)), ((1, 2, 16384), (128, 1, 2)),
+                            ((4, 32, 8192), (64, 4, 32)), ((1, 1, 1000), (8, 1, 1))):
+        assert schedule.bwd_grid(B, H, N, 128) == want
+    # The pages' grid has one block per column of the tile grid: the column
+    # ranges of the blocks cover every key exactly once.
+    for N in (1, 127, 128, 129, 255, 256, 257, 1000):
+        nb = schedule.bwd_grid(1, 1, N, 128)[0]
+        keys = [k for n in range(nb) for k in range(n * 128, min(N, (n + 1) * 128))]
+        assert keys == list(range(N))
+        assert nb * 128 >= N > (nb - 1) * 128
+
+
 @pytest.mark.parametrize("N,bm,bn", [(1, 128, 128), (127, 64, 128), (300, 128, 128),
                                      (1000, 256, 128), (777, 64, 32)])
 def test_tile_ranges_match_element_level_brute_force(N, bm, bn):
@@ -98,6 +115,68 @@ def test_num_splits_follows_the_stated_rule():
             eff = [schedule.split_utilisation(workers, 152, c) for c in range(1, top + 1)]
             assert eff[s - 1] >= 0.95 * max(eff)
             assert all(eff[c - 1] < 0.95 * max(eff) for c in range(1, s))
+
+
+def test_greedy_makespan_by_hand():
+    # [3, 3, 2, 2, 2] on 2 SMs: 3 | 3, then 2 -> 5 | 3, 2 -> 5 | 5, 2 -> 7 | 5.
+    assert schedule.greedy_makespan([3, 3, 2, 2, 2], 2) == 7
+    # One long CTA and five short ones: the short ones fill the other SM.
+    assert schedule.greedy_makespan([5, 1, 1, 1, 1, 1], 2) == 5
+    assert schedule.greedy_makespan([4, 4, 4], 4) == 4
+    assert schedule.greedy_makespan([], 3) == 0
+
+
+def test_split_launch_order():
+    """Blocks in the given order, each block's parts in order, heads fastest;
+    a block with one part is not marked split."""
+    got = schedule.split_launch([4, 2], 2, 2)
+    assert got == [(2, True), (2, True), (2, True), (2, True), (2, False), (2, False)]
+    assert schedule.split_launch([5], 1, 2) == [(2, True), (3, True)]
+    assert schedule.split_launch([3, 1], 1, 1) == [(3, False), (1, False)]
+
+
+def test_makespan_utilisation_by_hand():
+    """Two causal row blocks of 4 and 2 tiles, one head, 4 SMs, no costs:
+    s = 1 runs [4, 2] (makespan 4, 6 / 16); s = 2 cuts only the first block,
+    [2, 2, 2] (makespan 2, 6 / 8); s = 4 gives [1, 1, 1, 1, 1, 1] (makespan 2,
+    6 / 8). With the fixed costs (1 per CTA, 6 more per split part): s = 1
+    costs [5, 3] (6 / 20); s = 2 costs [9, 9, 3] (6 / 36); s = 4 costs six
+    CTAs of 8 on 4 SMs (makespan 16, 6 / 64)."""
+    u = schedule.split_utilisation_makespan
+    assert u([4, 2], 1, 4, 1, 0, 0) == 6 / 16
+    assert u([4, 2], 1, 4, 2, 0, 0) == 6 / 8
+    assert u([4, 2], 1, 4, 4, 0, 0) == 6 / 8
+    assert u([4, 2], 1, 4, 1) == 6 / 20
+    assert u([4, 2], 1, 4, 2) == 6 / 36
+    assert u([4, 2], 1, 4, 4) == 6 / 64
+    # Splitting pays when one long block would keep one SM busy alone:
+    # 64 tiles on 4 SMs, s = 1, 2, 4 take 65, 39 (2 x 32 + 7) and 23 (4 x 16 + 7).
+    assert [u([64], 1, 4, c) for c in (1, 2, 4)] == [64 / 260, 64 / 156, 64 / 92]
+    assert schedule.num_splits_makespan([64], 1, 4, 128) == 4
+    assert schedule.num_splits_makespan([4, 2], 1, 4, 128) == 1
+
+
+def test_makespan_reading_reduces_to_waves():
+    """Equal workers and no costs: the makespan utilisation is the filled
+    fraction of the waves."""
+    for workers in (1, 7, 64, 152, 153, 300):
+        for sms in (4, 152):
+            for s in (1, 2, 3):
+                got = schedule.split_utilisation_makespan([6] * workers, 1, sms, s, 0, 0)
+                assert got == pytest.approx(schedule.split_utilisation(workers, sms, s)), (workers, sms, s)
+
+
+def test_makespan_rule_follows_the_stated_rule():
+    """The choice has utilisation >= 0.95 of the best candidate and no smaller
+    candidate has, over causal and equal block sets."""
+    for tiles in ([8, 6, 4, 2], [16] * 3, [32, 30, 28, 26, 24, 22, 20, 18, 16, 14, 12, 10, 8, 6, 4, 2]):
+        for BH in (1, 2, 5):
+            for sms in (8, 16, 152):
+                s = schedule.num_splits_makespan(tiles, BH, sms, 128)
+                top = min(128, sms, max(tiles))
+                eff = [schedule.split_utilisation_makespan(tiles, BH, sms, c) for c in range(1, top + 1)]
+                assert eff[s - 1] >= 0.95 * max(eff)
+                assert all(eff[c - 1] < 0.95 * max(eff) for c in range(1, s))
 
 
 @pytest.mark.parametrize("j0,j1", [(0, 1), (0, 5), (3, 17), (0, 128)])
