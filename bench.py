@@ -46,14 +46,20 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--cpu-sample-heads", type=int, default=3)
-    p.add_argument("--fwd-splits", default="1",
-                   help="K/V parts per forward worker: an integer or 'auto' (fa2_fwd_split)")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the forward/backward lines of the other configurations")
+    p.add_argument("--fwd-splits", default="auto",
+                   help="K/V parts per forward worker: an integer, or 'auto' for the library's "
+                        "rule (the default of forward())")
     p.add_argument("--record-traffic", metavar="NCU_REP", default=None,
                    help="write profiles/traffic.json from an ncu report of --workload "
                         "(dram__bytes_read.sum + dram__bytes_write.sum per kernel launch, scaled "
                         "to the headline workload by heads) and exit")
     p.add_argument("--e2e-heads-per-chunk", type=int, default=0,
                    help="heads per pipelined chunk of the end-to-end leg (fa2_step_host; 0 = auto)")
+    p.add_argument("--bwd", default="split", choices=["split", "atomic"],
+                   help="backward: split (fa2_bwd: dK/dV workers and dQ workers, no atomics) or "
+                        "atomic (fa2_bwd_atomic: column workers with fp32 dQ reduce-adds)")
     p.add_argument("--fwd-order", default="fa2", choices=["fa2", "kv_outer"],
                    help="forward loop order: fa2 (Q outer) or kv_outer (the FlashAttention-1 "
                         "order, fa2_fwd_kv_outer), for measuring the loop order")
@@ -152,8 +158,8 @@ def job_tflops(flops_per_rank_step: float, world: int, steps: int, ms: float) ->
 
 def cpu_baseline(w, heads: int):
     """The fp64 oracle, as it stands, on a bounded sample of the workload: the
-    first `heads` heads, forward + backward. Returns TFLOP/s in the metric's
-    FLOP convention."""
+    first `heads` heads, forward and backward timed separately. Returns
+    TFLOP/s in the metric's FLOP convention (fwd+bwd, and each on its own)."""
     import torch
 
     import oracle
@@ -164,14 +170,19 @@ def cpu_baseline(w, heads: int):
     q, k, v, do = map(f, (q, k, v, do))
     t0 = time.perf_counter()
     oracle.forward(q, k, v, causal=w.causal, scale=w.scale)
+    t1 = time.perf_counter()
     oracle.backward(q, k, v, do, causal=w.causal, scale=w.scale)
-    dt = time.perf_counter() - t0
-    per_head = (w.fwd_flops() + w.bwd_flops()) / (w.B * w.H)
-    return {"value": per_head * heads / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
-            "kind": "oracle",
-            "sample": f"{heads} of {w.B * w.H} heads (N={w.N}, d={w.d}), fwd+bwd in fp64 NumPy, "
-                      f"{dt:.2f} s",
-            "seconds": dt}
+    t2 = time.perf_counter()
+    fwd_s, bwd_s = t1 - t0, t2 - t1
+    per_head_f = w.fwd_flops() / (w.B * w.H)
+    per_head_b = w.bwd_flops() / (w.B * w.H)
+    return {"value": (per_head_f + per_head_b) * heads / (fwd_s + bwd_s) / 1e12, "unit": UNIT,
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} heads (N={w.N}, d={w.d}), fwd and bwd in fp64 "
+                      f"NumPy, {fwd_s:.2f} s + {bwd_s:.2f} s",
+            "fwd_tflops": per_head_f * heads / fwd_s / 1e12,
+            "bwd_tflops": per_head_b * heads / bwd_s / 1e12,
+            "seconds": fwd_s + bwd_s}
 
 
 def run_reference(args, w, rank, world):
@@ -200,8 +211,12 @@ def run_reference(args, w, rank, world):
 
 TRAFFIC_FILES = {
     "fa2_fwd_kernel": ["fa2_fwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
-    "fa2_bwd_main_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
-    "fa2_bwd_pre_kernel": ["fa2_bwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_main_kernel": ["fa2_bwd.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_fused_kernel": ["fa2_bwd_fused.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh",
+                             "sm103_ptx.cuh"],
+    "fa2_bwd_pre_kernel": ["fa2_bwd.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_dq_convert_kernel": ["fa2_bwd_fused.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh",
+                                  "sm103_ptx.cuh"],
 }
 
 
@@ -263,6 +278,94 @@ def record_traffic(rep: str, measured) -> None:
     print(json.dumps({k: v["bytes_per_launch"] for k, v in kernels.items()}))
 
 
+DETAIL_CONFIGS = ["causal_bf16_b2h4_n1024_d64", "bf16_b8h16_n2048_d128",
+                  "causal_bf16_b8h16_n2048_d128", "causal_bf16_b1h2_n16384_d128"]
+
+
+def time_fwd_bwd(fa2, lib, w, dev, steps: int, warmup: int, fwd_splits):
+    """Mean forward and backward times (ms, CUDA events on the launching
+    stream) of workload w, and the split count the forward used. Inputs that
+    fit in L2 get a 256 MiB buffer overwritten before every step, outside the
+    events. fwd_splits: an integer, or "auto" for the library's own choice
+    (the product default of forward())."""
+    import torch
+
+    from exact_attention_64_gb300.workloads import workload_inputs
+
+    B, H, N, d = w.B, w.H, w.N, w.d
+    dt_code = 1 if w.dtype == "bf16" else 0
+    q, k, v, do = (t.to(dev) for t in workload_inputs(w))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa2.bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    causal = int(w.causal)
+    if fwd_splits == "auto":
+        fwd_splits = fa2.num_splits(B, H, N, d, w.causal,
+                                    torch.cuda.get_device_properties(dev).multi_processor_count)
+    fwd_splits = int(fwd_splits)
+    split_bytes = lib.fa2_fwd_split_workspace_size(B, H, N, d, fwd_splits) if fwd_splits > 1 else 0
+    split_ws = torch.empty(max(split_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        if fwd_splits > 1:
+            c = lib.fa2_fwd_split(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), B, H, N, d, causal, w.scale, dt_code, fwd_splits,
+                                  split_ws.data_ptr(), split_bytes, sp)
+        else:
+            c = lib.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, N, d, causal, w.scale, dt_code, sp)
+        if c:
+            raise fa2.FA2Error("fa2_fwd", c)
+
+    def bwd():
+        c = lib.fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+                        causal, w.scale, dt_code, ws.data_ptr(), ws_bytes, sp)
+        if c:
+            raise fa2.FA2Error("fa2_bwd", c)
+
+    step_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, do, o, dq, dk, dv))
+    flush = step_bytes <= 2 * L2_BYTES
+    scratch = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev) if flush else None
+    for _ in range(warmup):
+        fwd()
+        bwd()
+    E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    ev = [(E(), E(), E()) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for s, (a, b, c) in enumerate(ev):
+        if flush:
+            scratch.fill_(s & 0xFF)
+        a.record(stream)
+        fwd()
+        b.record(stream)
+        bwd()
+        c.record(stream)
+    torch.cuda.synchronize()
+    st = fa2.device_status()
+    if st != 0:
+        raise SystemExit(f"device status {fa2.status_string(st)} while timing {w.name}")
+    t_f = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    t_b = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    return t_f, t_b, fwd_splits, flush
+
+
+def config_line(fa2, lib, w, dev, steps, warmup, peak, fwd_splits="auto"):
+    """Forward and backward TFLOP/s of workload w and their fractions of the
+    burst bf16 peak (a launch of microseconds to milliseconds is a burst)."""
+    t_f, t_b, S, flush = time_fwd_bwd(fa2, lib, w, dev, steps, warmup, fwd_splits)
+    f_tf = w.fwd_flops() / (t_f * 1e-3) / 1e12
+    b_tf = w.bwd_flops() / (t_b * 1e-3) / 1e12
+    return {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal, "dtype": w.dtype,
+            "fwd_splits": S, "fwd_ms": t_f, "bwd_ms": t_b, "fwd_tflops": f_tf,
+            "bwd_tflops": b_tf, "fwd_frac_of_peak": f_tf / peak, "bwd_frac_of_peak": b_tf / peak,
+            "l2_flushed": flush}
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -303,7 +406,8 @@ def main():
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = fa2.bwd_workspace_size(B, H, N, d)
+    det = args.bwd == "split"
+    ws_bytes = fa2.bwd_workspace_size(B, H, N, d, not det)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -344,10 +448,10 @@ def main():
         if ev_handles is not None:
             arr = (ctypes.c_void_p * 4)(*ev_handles)
             evp = ctypes.cast(arr, ctypes.c_void_p)
-        c = lib.fa2_bwd_timed(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                              lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                              dv.data_ptr(), B, H, N, d, causal, scale, dt_code, ws.data_ptr(),
-                              ws_bytes, evp, sp)
+        fn = lib.fa2_bwd_timed if det else lib.fa2_bwd_atomic_timed
+        c = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+               do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal,
+               scale, dt_code, ws.data_ptr(), ws_bytes, evp, sp)
         if c:
             raise fa2.FA2Error("fa2_bwd", c)
 
@@ -355,8 +459,9 @@ def main():
         fwd()
         bwd()
     torch.cuda.synchronize()
-    if fa2.device_status() != 0:
-        raise SystemExit("device status error during warm-up")
+    st = fa2.device_status()
+    if st != 0:
+        raise SystemExit(f"device status {fa2.status_string(st)} during warm-up")
 
     # ---- timed region: K steps, per-kernel events on the launching stream ----
     E = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
@@ -376,28 +481,37 @@ def main():
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    nvtx = torch.cuda.nvtx
     with ClockSampler(local) as clk:
+        nvtx.range_push("timed region")
         t0.record(stream)
         for s in range(args.steps):
             if flush:
                 scratch.fill_(s & 0xFF)
             fwd_ev[s][0].record(stream)
+            nvtx.range_push("forward")
             fwd()
+            nvtx.range_pop()
             fwd_ev[s][1].record(stream)
+            nvtx.range_push("backward")
             bwd([e.cuda_event for e in bwd_ev[s]])
+            nvtx.range_pop()
         t1.record(stream)
         torch.cuda.synchronize()
+        nvtx.range_pop()
     if world > 1:
         dist.barrier()
     if flush:
         elapsed_ms = sum(f[0].elapsed_time(b[3]) for f, b in zip(fwd_ev, bwd_ev))
     else:
         elapsed_ms = t0.elapsed_time(t1)
-    if fa2.device_status() != 0:
-        raise SystemExit("device status error in the timed region")
+    st = fa2.device_status()
+    if st != 0:
+        raise SystemExit(f"device status {fa2.status_string(st)} in the timed region")
     t_fwd = [a.elapsed_time(b) for a, b in fwd_ev]
     t_pre = [e[0].elapsed_time(e[1]) for e in bwd_ev]
     t_kv = [e[1].elapsed_time(e[2]) for e in bwd_ev]
+    t_conv = [e[2].elapsed_time(e[3]) for e in bwd_ev]
     elapsed_ms = slowest_rank_ms(elapsed_ms, dist if world > 1 else None, dev)
 
     flops_step = w.fwd_flops() + w.bwd_flops()
@@ -408,13 +522,21 @@ def main():
     # N x N x d GEMM units (S, PV) and the backward as five (2.5x). The
     # backward's main launch runs the dK/dV workers (S^T, dP^T, dV, dK: four
     # units) and the dQ workers (dQ, plus the recomputed S and dP that the
-    # convention does not count): five units credited.
+    # convention does not count): five units credited. fa2_bwd_atomic's main
+    # launch (the column workers) executes exactly the five. The
+    # preprocessing pass reads O and dO and writes D and L*log2e (and, for
+    # fa2_bwd_atomic, zeroes the fp32 dQ accumulator); that variant's
+    # conversion reads the accumulator and writes dQ.
     fw = w.fwd_flops()
+    n_pad = -(-N // 128) * 128
+    pre_bytes = B * H * N * (2 * d * 2 + 4 + 8) + (0 if det else B * H * n_pad * d * 4)
     kernels = {
         ("fa1_order_fwd_kernel" if kv_outer else "fa2_fwd_kernel"): (mean(t_fwd), fw, "tensor"),
-        "fa2_bwd_main_kernel": (mean(t_kv), 2.5 * fw, "tensor"),
-        "fa2_bwd_pre_kernel": (mean(t_pre), B * H * N * (2 * d * 2 + 4 + 8), "hbm"),
+        ("fa2_bwd_main_kernel" if det else "fa2_bwd_fused_kernel"): (mean(t_kv), 2.5 * fw, "tensor"),
+        "fa2_bwd_pre_kernel": (mean(t_pre), pre_bytes, "hbm"),
     }
+    if not det:
+        kernels["fa2_bwd_dq_convert_kernel"] = (mean(t_conv), B * H * N * d * (4 + 2), "hbm")
     dom = max(kernels, key=lambda n: kernels[n][0])
     ms, work, bound = kernels[dom]
     traffic = None
@@ -425,11 +547,13 @@ def main():
                 and ent.get("source_sha") == source_sha(ent.get("files", []))):
             traffic = ent.get("bytes_per_launch")
     if bound == "tensor":
+        # The timed region is a fraction of a second of back-to-back launches
+        # of milliseconds each, not a seconds-long loop: the burst peak applies.
         achieved = work / (ms * 1e-3) / 1e12
-        peak = pk["bf16_sustained"]
+        peak = pk["bf16"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom,
-                "peak_kind": f"bf16 sustained ({pk['source']})"}
+                "peak_kind": f"bf16 burst ({pk['source']})"}
     else:
         achieved = work / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -438,7 +562,7 @@ def main():
     tot = sum(x[0] for x in kernels.values())
     per_kernel = {n: {"ms": t, "share": t / tot} for n, (t, _, _) in kernels.items()}
     fwd_tf = fw / (mean(t_fwd) * 1e-3) / 1e12
-    bwd_tf = w.bwd_flops() / ((mean(t_pre) + mean(t_kv)) * 1e-3) / 1e12
+    bwd_tf = w.bwd_flops() / ((mean(t_pre) + mean(t_kv) + mean(t_conv)) * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -469,21 +593,44 @@ def main():
         if world > 1:
             dist.barrier()
         a, b = E(), E()
+        nvtx.range_push("end to end (host buffers)")
         a.record(stream)
         for _ in range(args.steps):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
+        nvtx.range_pop()
+        st = fa2.device_status()
+        if st != 0:
+            raise SystemExit(f"device status {fa2.status_string(st)} in the end-to-end leg")
         e_ms = slowest_rank_ms(a.elapsed_time(b), dist if world > 1 else None, dev)
         e2e = {"value": job_tflops(flops_step, world, args.steps, e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / args.steps, "api": "fa2_step_host",
                "heads_per_chunk": hpc or -(-(B * H) // 8)}
 
+    # ---- every other configuration of the metric, causal and not ----
+    configs = {}
+    if not args.no_configs and args.workload is None:
+        for name in DETAIL_CONFIGS:
+            cw = WORKLOADS[name]
+            configs[name] = config_line(fa2, lib, cw, dev, 10, 3, pk["bf16"])
+            if cw.causal and configs[name]["fwd_splits"] != 1:
+                unsplit = config_line(fa2, lib, cw, dev, 10, 3, pk["bf16"], fwd_splits=1)
+                configs[name]["fwd_unsplit"] = {k: unsplit[k] for k in
+                                                ("fwd_ms", "fwd_tflops", "fwd_frac_of_peak")}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_sample_heads)
         cpu.pop("seconds", None)
+        if configs:
+            # The oracle on one head of every other configuration, forward and
+            # backward timed separately.
+            cpu["configs"] = {}
+            for name in configs:
+                c1 = cpu_baseline(WORKLOADS[name], 1)
+                cpu["configs"][name] = {k: c1[k] for k in ("fwd_tflops", "bwd_tflops", "sample")}
 
     l2_note = (f"L2 flushed between steps (256 MiB written; {step_bytes / 2**20:.0f} MiB touched "
                f"per step fits in L2); step time = sum of per-step event spans" if flush else
@@ -495,17 +642,20 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "q_std": w.q_std, "parallelism": f"head-sharded replicas x{world}",
-                   "l2": l2_note, "fwd_splits": fwd_splits, "fwd_order": args.fwd_order},
+                   "l2": l2_note, "fwd_splits": fwd_splits, "fwd_order": args.fwd_order,
+                   "bwd": args.bwd},
         "detail": {"fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
-                   "fwd_frac_of_peak": fwd_tf / pk["bf16_sustained"],
-                   "bwd_frac_of_peak": bwd_tf / pk["bf16_sustained"],
-                   "peak_tflops": pk["bf16_sustained"], "per_kernel": per_kernel},
+                   "fwd_frac_of_peak": fwd_tf / pk["bf16"],
+                   "bwd_frac_of_peak": bwd_tf / pk["bf16"],
+                   "peak_tflops": pk["bf16"], "peak_kind": f"bf16 burst ({pk['source']})",
+                   "per_kernel": per_kernel, "configs": configs},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        # forward, backward preprocessing, backward main launch (dK/dV and dQ
-        # workers) per step; a split forward adds a counter memset, not a kernel
-        "gpu_launches": 3 * args.steps,
+        # per step: the forward (a split forward adds a counter memset, not a
+        # kernel), the backward's preprocessing, its main launch and, for
+        # fa2_bwd_atomic, the dQ conversion
+        "gpu_launches": (3 if det else 4) * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0:

@@ -80,9 +80,14 @@ def load_library() -> ctypes.CDLL:
         "fa2_step_host_workspace_size": (sz, [i, i, i, i, i]),
         "fa2_num_splits": (i, [i, i, i, i, i, i]),
         "fa2_bwd_workspace_size": (sz, [i, i, i, i]),
+        "fa2_bwd_atomic_workspace_size": (sz, [i, i, i, i]),
         "fa2_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]),
+        "fa2_bwd_atomic": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz,
+                               vp]),
         "fa2_bwd_timed": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp,
                               vp]),
+        "fa2_bwd_atomic_timed": (i, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp,
+                                     sz, vp, vp]),
         "fa2_get_device_status": (i, [vp]),
         "fa2_status_string": (ctypes.c_char_p, [i]),
         "fa2_fwd_grid": (i, [i, i, i, _c_int_p, _c_int_p]),
@@ -147,14 +152,16 @@ def num_splits(B: int, H: int, N: int, d: int, causal: bool, num_sms: int) -> in
 
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
-            num_splits: int | str = 1):
+            num_splits: int | str = "auto"):
     """O = softmax(scale * Q K^T [+ causal mask]) V and its logsumexp L.
 
     ``num_splits`` > 1 cuts each worker's K/V range into that many parts run by
-    separate CTAs and merges them (fa2_fwd_split); "auto" picks the count with
-    the library's rule for this GPU. k and v may have their own length N_k
-    (fa2_fwd_qk; causal mask top-left: query i sees keys 0..i). Returns
-    (o, lse): o like q, lse float32 [B, H, N] (natural log).
+    separate CTAs and merges them (fa2_fwd_split); "auto" (the default) takes
+    the library's rule for this GPU (fa2_num_splits), which keeps 1 unless the
+    unsplit launch leaves the SMs underused; 1 always runs fa2_fwd. k and v
+    may have their own length N_k (fa2_fwd_qk, never split; causal mask
+    top-left: query i sees keys 0..i). Returns (o, lse): o like q, lse
+    float32 [B, H, N] (natural log).
     """
     B, H, N, d = _shape(q)
     Nk = _shape(k)[2]
@@ -291,14 +298,18 @@ def forward_instrumented(q, k, v, causal=False, scale=None):
     return out, lse, counts
 
 
-def bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
-    return int(load_library().fa2_bwd_workspace_size(B, H, N, d))
+def bwd_workspace_size(B: int, H: int, N: int, d: int, atomic: bool = False) -> int:
+    lib = load_library()
+    if atomic:
+        return int(lib.fa2_bwd_atomic_workspace_size(B, H, N, d))
+    return int(lib.fa2_bwd_workspace_size(B, H, N, d))
 
 
 def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None,
-             dq=None, dk=None, dv=None, workspace=None):
+             dq=None, dk=None, dv=None, workspace=None, atomic: bool = False):
     """Gradients (dq, dk, dv) of the attention output given dO. k and v may
-    have their own length N_k (fa2_bwd_qk)."""
+    have their own length N_k (fa2_bwd_qk). ``atomic`` runs fa2_bwd_atomic,
+    the column-worker variant with fp32 dQ reduce-adds (equal lengths only)."""
     B, H, N, d = _shape(q)
     Nk = _shape(k)[2]
     dt = q.dtype
@@ -318,10 +329,20 @@ def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = No
     _check_tensor("dq", dq, (B, H, N, d), dt, dev)
     for name, t in (("dk", dk), ("dv", dv)):
         _check_tensor(name, t, (B, H, Nk, d), dt, dev)
-    need = bwd_workspace_size(B, H, N, d)
+    need = bwd_workspace_size(B, H, N, d, atomic)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     lib = load_library()
+    if atomic:
+        if Nk != N:
+            raise ValueError("fa2_bwd_atomic needs equal query and key lengths")
+        code = lib.fa2_bwd_atomic(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                  _DTYPES[dt], workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), _stream_ptr(dev))
+        _check("fa2_bwd_atomic", code)
+        return dq, dk, dv
     if Nk != N:
         code = lib.fa2_bwd_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                               lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(),

@@ -5,7 +5,12 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <functional>
+#include <map>
 #include <mutex>
+#include <queue>
+#include <tuple>
+#include <vector>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -22,6 +27,10 @@ cudaError_t launch_fa1_order_fwd(int d, bool bf16, bool causal, const CUtensorMa
 cudaError_t launch_bwd(int d, bool bf16, bool causal, const void* o, const void* dO,
                        const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
                        float* l2, cudaStream_t stream, cudaEvent_t* ev);
+cudaError_t launch_bwd_fused(int d, bool bf16, bool causal, const void* o, const void* dO,
+                             const float* lse, const CUtensorMap* maps, const BwdArgs& a, float* dsum,
+                             float* l2, float* dq_acc, void* dq, int num_sms, cudaStream_t stream,
+                             cudaEvent_t* ev);
 }  // namespace fa2
 
 namespace {
@@ -41,8 +50,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 std::mutex g_mu;
 EncodeTiledFn g_encode = nullptr;
 int g_arch_ok[kMaxDevices];        // 0 unknown, 1 sm_103, -1 other
+int g_num_sms[kMaxDevices];        // multiprocessor count, per device
 int* g_status_ptr[kMaxDevices];    // device address of g_device_status, per device
-int g_fault_kind = 0;              // armed by fa2_debug_arm_fault, consumed by the next fwd
+int g_fault_kind = 0;              // armed by fa2_debug_arm_fault, consumed by the next call of its kind
 unsigned long long g_fault_timeout_ns = 0;
 thread_local int g_last_cuda_error = 0;  // last cudaError_t behind an FA2_ERR_CUDA, per thread
 
@@ -74,6 +84,10 @@ int device_setup(int* dev_out, int** status_out) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     if (e != cudaSuccess) return cuda_fail(e);
     g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_num_sms[dev] = sms > 0 ? sms : 1;
   }
   if (g_arch_ok[dev] != 1) return FA2_ERR_ARCH;
   if (g_status_ptr[dev] == nullptr) {
@@ -132,6 +146,25 @@ int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dt
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     g_last_cuda_error = 1000 + static_cast<int>(r);  // driver codes offset by 1000
+    return FA2_ERR_CUDA;
+  }
+  return FA2_OK;
+}
+
+// 3-D tensor map over the fp32 dQ accumulator of fa2_bwd_atomic
+// [B*H][n_pad][d]: boxes of 32 rows x 32 columns (rows of 128 bytes, 128-byte
+// swizzled), the unit of its reduce-adds (one warp's rows).
+int make_map_dqacc(CUtensorMap* m, void* ptr, int BH, int n_pad, int d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(n_pad),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(n_pad) * d * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = 1000 + static_cast<int>(r);
     return FA2_ERR_CUDA;
   }
   return FA2_OK;
@@ -207,10 +240,13 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.part_done = part_done;
-  if (num_splits <= 1) {
+  {
+    // An armed failure-path fault is consumed by the next call of its kind:
+    // 1 by an unsplit forward, 2 by a split one; both make the producer skip
+    // the first V tile.
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_fault_kind != 0) {
-      a.fault = g_fault_kind;
+    if (g_fault_kind == (num_splits <= 1 ? 1 : 2)) {
+      a.fault = 1;
       a.timeout_ns = g_fault_timeout_ns;
       g_fault_kind = 0;
     }
@@ -226,6 +262,87 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     e = fa2::launch_fwd(d, dtype == FA2_BF16, causal != 0, tq, tk, tv, to, a,
                         static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA2_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------------------
+// The K/V split count ("大猿搬砖简记", thread-block section, the
+// num_splits_heuristic_fwd paragraph): the SM utilisation of every candidate
+// split count, the best of them, and the smallest candidate within 0.95 of the
+// best. Utilisation, which the page leaves undefined, is read as the fraction
+// of the SMs' time spent on K/V tiles: useful tiles / (num_sms * makespan)
+// when the launch's CTAs (row blocks longest first, each block's parts in
+// order, heads fastest) start in launch order on the SM that frees first, a
+// CTA taking its tiles plus kCtaCost, plus kPartCost more if its block is
+// split. The costs are in tiles, measured on GB300. Integer arithmetic up to
+// the one division per candidate, as in the fp64 reference of the rule.
+// ---------------------------------------------------------------------------
+constexpr long long kCtaCost = 1;
+constexpr long long kPartCost = 6;
+
+double split_utilisation_makespan(const std::vector<int>& tiles, int BH, int num_sms, int s) {
+  const int n_max = tiles.empty() ? 0 : tiles[0];
+  std::priority_queue<long long, std::vector<long long>, std::greater<long long>> free_at;
+  for (int k = 0; k < num_sms; ++k) free_at.push(0);
+  long long useful = 0;
+  for (const int n : tiles) {
+    const int p = fa2::fwd_num_parts(n, s, n_max);
+    for (int part = 0; part < p; ++part) {
+      int lo = 0, hi = 0;
+      fa2::fwd_part_range(n, p, part, &lo, &hi);
+      const long long cost = (hi - lo) + kCtaCost + (p > 1 ? kPartCost : 0);
+      for (int h = 0; h < BH; ++h) {
+        const long long t = free_at.top();
+        free_at.pop();
+        free_at.push(t + cost);
+        useful += hi - lo;
+      }
+    }
+  }
+  long long span = 0;
+  while (!free_at.empty()) {
+    span = std::max(span, free_at.top());
+    free_at.pop();
+  }
+  return span > 0 ? static_cast<double>(useful) / (static_cast<double>(num_sms) * span) : 1.0;
+}
+
+std::mutex g_split_mu;
+std::map<std::tuple<int, int, int, int>, int> g_split_cache;  // (BH, N, causal, SMs) -> count
+
+int num_splits_makespan(int BH, int N, int causal, int num_sms) {
+  const auto key = std::make_tuple(BH, N, causal, num_sms);
+  {
+    std::lock_guard<std::mutex> lock(g_split_mu);
+    const auto it = g_split_cache.find(key);
+    if (it != g_split_cache.end()) return it->second;
+  }
+  // Row blocks in launch order (causal: longest first) with their K/V tiles.
+  const int nm = fa2::fwd_num_m_blocks(N);
+  std::vector<int> tiles(nm);
+  for (int k = 0; k < nm; ++k)
+    tiles[k] = fa2::fwd_block_tiles(fa2::fwd_m_block_of(k, nm, causal), N, N, causal);
+  const int top = std::max(1, std::min(std::min(kMaxFwdSplits, num_sms), tiles[0]));
+  std::vector<double> eff(top + 1, 0.0);
+  double best = 0.0;
+  eff[1] = split_utilisation_makespan(tiles, BH, num_sms, 1);
+  int pick = 1;
+  // With utilisation >= 0.95 unsplit, 1 is the smallest candidate within 0.95
+  // of any best (<= 1): the other candidates need not be evaluated.
+  if (eff[1] < 0.95) {
+    for (int s = 1; s <= top; ++s) {
+      if (s > 1) eff[s] = split_utilisation_makespan(tiles, BH, num_sms, s);
+      best = std::max(best, eff[s]);
+    }
+    for (int s = 1; s <= top; ++s)
+      if (eff[s] >= 0.95 * best) {
+        pick = s;
+        break;
+      }
+  }
+  std::lock_guard<std::mutex> lock(g_split_mu);
+  if (g_split_cache.size() > 4096) g_split_cache.clear();
+  g_split_cache[key] = pick;
+  return pick;
 }
 
 }  // namespace
@@ -255,10 +372,9 @@ size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits) 
 
 int fa2_num_splits(int B, int H, int N, int d, int causal, int num_sms) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || (causal != 0 && causal != 1) ||
-      num_sms < 1)
+      num_sms < 1 || static_cast<long long>(B) * H > (1 << 30))
     return 0;
-  const int workers = B * H * fa2::fwd_num_m_blocks(N);
-  return fa2::fwd_num_splits(workers, num_sms, fa2::ceil_div(N, fa2::kTileRows), kMaxFwdSplits);
+  return num_splits_makespan(B * H, N, causal, num_sms);
 }
 
 int fa2_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -341,12 +457,23 @@ size_t fa2_bwd_workspace_size(int B, int H, int N, int d) {
   return 2 * align_up(bh * n_pad * 4, 256);
 }
 
+size_t fa2_bwd_atomic_workspace_size(int B, int H, int N, int d) {
+  const size_t rows = fa2_bwd_workspace_size(B, H, N, d);
+  if (rows == 0) return 0;
+  // ... followed by the fp32 dQ accumulator [B*H][N_pad][d].
+  const size_t n_pad = align_up(static_cast<size_t>(N), 128);
+  return rows + align_up(static_cast<size_t>(B) * H * n_pad * d * 4, 256);
+}
+
 namespace {
 // N: query length (q, o, dO, dq, lse); Nk: key length (k, v, dk, dv).
+// atomic = 0: the split backward (dK/dV workers and dQ workers in one launch,
+// no atomics, bit-reproducible); 1: the column workers with fp32 dQ
+// reduce-adds (fa2_bwd_atomic).
 int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int Nk, int d,
              int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
-             void* const* phase_events, void* stream) {
+             void* const* phase_events, void* stream, int atomic) {
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv) return FA2_ERR_INVALID_ARG;
   int st = check_common(B, H, N, d, causal, scale, dtype);
   if (st != FA2_OK) return st;
@@ -359,7 +486,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   for (void* p : out16)
     if (!aligned(p, 16)) return FA2_ERR_ALIGNMENT;
   if (!aligned(lse, 4)) return FA2_ERR_ALIGNMENT;
-  const size_t need = fa2_bwd_workspace_size(B, H, N, d);
+  const size_t need = atomic ? fa2_bwd_atomic_workspace_size(B, H, N, d)
+                             : fa2_bwd_workspace_size(B, H, N, d);
   if (workspace == nullptr || workspace_bytes < need) return FA2_ERR_WORKSPACE;
   if (!aligned(workspace, 256)) return FA2_ERR_ALIGNMENT;
   const size_t qb = static_cast<size_t>(B) * H * N * d * 2;   // q, o, dO, dq
@@ -383,8 +511,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   st = device_setup(&dev, &status);
   if (st != FA2_OK) return st;
   const int BH = B * H;
-  // Tensor maps: q, k, v, dO (loads), dk, dv, dq (stores); all 128-row boxes.
-  CUtensorMap maps[7];
+  // Tensor maps: q, k, v, dO (loads), dk, dv, dq (stores); all 128-row boxes;
+  // fa2_bwd_atomic adds the fp32 dQ accumulator (reduce-adds).
+  CUtensorMap maps[8];
   const void* src[7] = {q, k, v, dO, dk, dv, dq};
   const int rows[7] = {N, Nk, Nk, N, Nk, Nk, N};
   for (int i = 0; i < 7; ++i)
@@ -393,6 +522,9 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   const size_t lbytes_pad = align_up(static_cast<size_t>(BH) * n_pad * 4, 256);
   float* dsum = static_cast<float*>(workspace);
   float* l2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + lbytes_pad);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * lbytes_pad);
+  if (atomic && make_map_dqacc(&maps[7], dq_acc, BH, static_cast<int>(n_pad), d) != FA2_OK)
+    return FA2_ERR_CUDA;
   fa2::BwdArgs a{};
   a.l2_pad = l2;
   a.dsum_pad = dsum;
@@ -405,11 +537,26 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   a.scale_log2 = scale * 1.4426950408889634f;
   a.status = status;
   a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
+  a.fault = 0;
+  {
+    // Kind 3 is consumed by the next backward of either kind: the producer of
+    // the K/V column workers skips the first dO tile. Kind 4 by the next
+    // fa2_bwd: the dQ workers' producer skips the first V tile.
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_fault_kind == 3 || (g_fault_kind == 4 && !atomic)) {
+      a.fault = g_fault_kind - 2;
+      a.timeout_ns = g_fault_timeout_ns;
+      g_fault_kind = 0;
+    }
+  }
   (void)cudaGetLastError();  // see fwd_impl
-  const cudaError_t e = fa2::launch_bwd(
-      d, dtype == FA2_BF16, causal != 0, o, dO, lse, maps, a, dsum, l2,
-      static_cast<cudaStream_t>(stream),
-      reinterpret_cast<cudaEvent_t*>(const_cast<void**>(phase_events)));
+  cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(phase_events));
+  const cudaError_t e =
+      atomic ? fa2::launch_bwd_fused(d, dtype == FA2_BF16, causal != 0, o, dO, lse, maps, a, dsum,
+                                     l2, dq_acc, dq, g_num_sms[dev], static_cast<cudaStream_t>(stream),
+                                     ev)
+             : fa2::launch_bwd(d, dtype == FA2_BF16, causal != 0, o, dO, lse, maps, a, dsum, l2,
+                               static_cast<cudaStream_t>(stream), ev);
   return e == cudaSuccess ? FA2_OK : cuda_fail(e);
 }
 }  // namespace
@@ -419,7 +566,23 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
                   void* const* phase_events, void* stream) {
   return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, causal, scale, dtype, workspace,
-                  workspace_bytes, phase_events, stream);
+                  workspace_bytes, phase_events, stream, 0);
+}
+
+int fa2_bwd_atomic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                   void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, causal, scale, dtype, workspace,
+                  workspace_bytes, nullptr, stream, 1);
+}
+
+int fa2_bwd_atomic_timed(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, int causal, float scale, int dtype, void* workspace,
+                         size_t workspace_bytes, void* const* phase_events, void* stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, N, N, d, causal, scale, dtype, workspace,
+                  workspace_bytes, phase_events, stream, 1);
 }
 
 int fa2_bwd_qk(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -427,7 +590,7 @@ int fa2_bwd_qk(const void* q, const void* k, const void* v, const void* o, const
                int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
                void* stream) {
   return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, B, H, Nq, Nk, d, causal, scale, dtype,
-                  workspace, workspace_bytes, nullptr, stream);
+                  workspace, workspace_bytes, nullptr, stream, 0);
 }
 
 int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -496,8 +659,8 @@ int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_
 int fa2_last_cuda_error(void) { return g_last_cuda_error; }
 
 int fa2_debug_arm_fault(int kind, int timeout_ms) {
-  if (kind != 0 && kind != 1) return FA2_ERR_INVALID_ARG;
-  if (kind == 1 && (timeout_ms < 1 || timeout_ms > 5000)) return FA2_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 4) return FA2_ERR_INVALID_ARG;
+  if (kind != 0 && (timeout_ms < 1 || timeout_ms > 5000)) return FA2_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lock(g_mu);
   g_fault_kind = kind;
   g_fault_timeout_ns = static_cast<unsigned long long>(timeout_ms) * 1000000ull;

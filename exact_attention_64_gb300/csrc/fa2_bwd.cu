@@ -27,12 +27,10 @@
 //                                    dQ += dS K_j                      (TS, A from TMEM, M=128 queries, N=d)
 // with P = exp2(S * scale*log2e - L*log2e) and dS = P o (dP - D).
 #include <cuda_fp16.h>
-#include "fa2_common.cuh"
+#include "fa2_bwd_parts.cuh"
 #include "../../include/fa2.h"
 
 namespace fa2 {
-
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
@@ -126,11 +124,15 @@ __device__ __forceinline__ float dot8(uint4 x, uint4 y) {
 // and each warp keeps kPrePasses passes of loads in flight before reducing.
 constexpr int kPrePasses = 4;
 
+// With dq_acc (the fused backward's fp32 dQ accumulator, [BH][n_pad][D]), the
+// same pass also zeroes it, padding rows included: each lane clears the D/LPR
+// floats of its row that line up with its 8 elements of O.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256)
     fa2_bwd_pre_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                        const float* __restrict__ lse, float* __restrict__ dsum_pad,
-                       float* __restrict__ l2_pad, int BH, int N, int n_pad) {
+                       float* __restrict__ l2_pad, float* __restrict__ dq_acc, int BH, int N,
+                       int n_pad) {
   constexpr int LPR = D / 8;     // lanes per row
   constexpr int RPW = 32 / LPR;  // rows per warp per pass
   constexpr int U = kPrePasses;
@@ -165,118 +167,11 @@ __global__ void __launch_bounds__(256)
         dsum_pad[r] = valid[u] ? acc : 0.f;
         l2_pad[r] = valid[u] ? lse[src[u]] * kLog2e : 0.f;
       }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Shared pieces of the two tensor-core kernels
-// ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                          int row, int bh) {
-#pragma unroll
-  for (int s = 0; s < D / 64; ++s)
-    tma_load_3d(dst + s * BwdCfg<D>::SLAB_BYTES, map, bar, s * 64, row, bh);
-}
-
-// D[tmem] = A B^T over the head dimension: M=128 rows of A, N=128 rows of B,
-// K=d. Both tiles K-major, 128-byte swizzled (the forward's Q K^T form).
-// Like every MMA helper here, issued by a converged warp (one lane elected).
-template <int D, bool BF16>
-__device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
-  constexpr uint32_t idesc = make_idesc_f16(128, 128, BF16, false, false);
-#pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk / 4) * BwdCfg<D>::SLAB_BYTES + (kk % 4) * 32;
-    const uint64_t ad = make_sdesc_sw128(a_smem + off, 16, 1024);
-    const uint64_t bd = make_sdesc_sw128(b_smem + off, 16, 1024);
-    umma_ss_warp(d_tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
-  }
-}
-
-// D[tmem] (+)= A[tmem] X with A = 128 x 128 16-bit pairs in TMEM and X a
-// 128-row tile [row][d] in shared memory (MN-major for this product; the
-// forward's P V form). a_col(kk) gives the TMEM column of A's 16-row block kk.
-template <int D, bool BF16, typename ACol>
-__device__ __forceinline__ void mma_tmem_x_tile(uint32_t d_tmem, ACol a_col, uint32_t x_smem,
-                                                bool accumulate) {
-  constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
-#pragma unroll
-  for (int kk = 0; kk < kTileRows / 16; ++kk) {
-    const uint64_t bd = make_sdesc_sw128(x_smem + kk * 2048, BwdCfg<D>::SLAB_BYTES, 1024);
-    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-    umma_ts_warp(d_tmem, a_col(kk), bd, idesc, acc);
-  }
-}
-
-// P^T for 32 query columns q_first.. of key row kg (dK/dV workers):
-// p[c] = exp2(S^T[c] * scale*log2e + nl_cols[c]), nl_cols = -(L*log2e) in registers. With MASK, pairs outside the
-// sequence or with key > query (causal) get 0. MASK is a template parameter so
-// that tiles off the diagonal run a loop with no per-element branches, which
-// would otherwise keep the exponentials from overlapping.
-template <bool MASK, bool CAUSAL>
-__device__ __forceinline__ void dkdv_p_cols(const uint32_t (&sv)[32], const float* nl_cols, float sl2,
-                                            int kg, int q_first, int Nq, int Nk, float* p) {
-#pragma unroll
-  for (int c = 0; c < 32; c += 2) {
-    const float2 x = f2_fma(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                            make_float2(sl2, sl2), make_float2(nl_cols[c], nl_cols[c + 1]));
-    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-    if constexpr (MASK) {
-      const int q0 = q_first + c;
-      p0 = (kg >= Nk || q0 >= Nq || (CAUSAL && kg > q0)) ? 0.f : p0;
-      p1 = (kg >= Nk || q0 + 1 >= Nq || (CAUSAL && kg > q0 + 1)) ? 0.f : p1;
-    }
-    p[c] = p0;
-    p[c + 1] = p1;
-  }
-}
-
-// dS for 64 key columns of query row my_row (dQ workers), packed to 16-bit
-// pairs: dS = P o (dP - D) with P = exp2(S * scale*log2e - L*log2e). With MASK,
-// keys at or past lim and rows past the sequence get P = 0. Column pairs use
-// packed fp32 (f32x2) arithmetic.
-template <bool MASK, bool BF16>
-__device__ __forceinline__ void dq_ds_cols(const uint32_t (&s)[64], const uint32_t (&dp)[64], float sl2,
-                                           float l2, float dsum, int kc0, int lim, bool row_ok,
-                                           uint32_t (&dsp)[32]) {
-  const float2 sl2x2 = make_float2(sl2, sl2), nl2 = make_float2(-l2, -l2);
-  const float2 dsum2 = make_float2(dsum, dsum);
-#pragma unroll
-  for (int c = 0; c < 64; c += 2) {
-    const float2 x = f2_fma(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nl2);
-    float p0 = ex2_approx(x.x), p1 = ex2_approx(x.y);
-    if constexpr (MASK) {
-      p0 = (!row_ok || kc0 + c >= lim) ? 0.f : p0;
-      p1 = (!row_ok || kc0 + c + 1 >= lim) ? 0.f : p1;
-    }
-    const float2 ds = f2_mul(make_float2(p0, p1),
-                             f2_sub(make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), dsum2));
-    dsp[c / 2] = pack_x2<BF16>(ds.x, ds.y);
-  }
-}
-
-// Stage a 128 x d fp32 TMEM accumulator (this thread's lane = row r) as 16-bit
-// rows, multiplied by mul, into a 128-byte-swizzled tile in shared memory.
-template <int D, bool BF16>
-__device__ __forceinline__ void stage_rows(uint8_t* stage, uint32_t t_src, int r, float mul) {
-#pragma unroll
-  for (int c = 0; c < D; c += 32) {
-    uint32_t x[32];
-    tmem_ld_32x32b_x32(t_src + c, x);
-    tmem_wait_ld();
-    reg_fence(x);
-    const int slab = c / 64, chunk0 = (c % 64) / 8;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint4 val;
-      val.x = pack_x2<BF16>(__uint_as_float(x[8 * k + 0]) * mul, __uint_as_float(x[8 * k + 1]) * mul);
-      val.y = pack_x2<BF16>(__uint_as_float(x[8 * k + 2]) * mul, __uint_as_float(x[8 * k + 3]) * mul);
-      val.z = pack_x2<BF16>(__uint_as_float(x[8 * k + 4]) * mul, __uint_as_float(x[8 * k + 5]) * mul);
-      val.w = pack_x2<BF16>(__uint_as_float(x[8 * k + 6]) * mul, __uint_as_float(x[8 * k + 7]) * mul);
-      *reinterpret_cast<uint4*>(stage + slab * BwdCfg<D>::SLAB_BYTES + r * 128 +
-                                (((chunk0 + k) ^ (r & 7)) * 16)) = val;
+      if (dq_acc != nullptr && r < total) {
+        float4* z = reinterpret_cast<float4*>(dq_acc + r * D + li * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -361,6 +256,7 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
         const int q0 = (i_begin + i) * kTileRows;
         mbar_arrive_expect_tx(&sh.q_full[st], C::TILE_BYTES);
         load_tile<D>(smem + C::OFF_STR0 + st * C::TILE_BYTES, &tm_q, &sh.q_full[st], q0, bh);
+        if (a.fault == 1 && i == 0) continue;  // failure-path test: dO_0 never arrives
         mbar_arrive_expect_tx(&sh.do_full[st], C::TILE_BYTES);
         load_tile<D>(smem + C::OFF_STR1 + st * C::TILE_BYTES, &tm_do, &sh.do_full[st], q0, bh);
       }
@@ -368,7 +264,8 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
         if (n_steps > 0) mbar_wait_drain(&sh.kv_full, 0, a.timeout_ns);
         for (int ii = max(0, i - C::NS); ii < i; ++ii) {
           mbar_wait_drain(&sh.q_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
-          mbar_wait_drain(&sh.do_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
+          if (!(a.fault == 1 && ii == 0))
+            mbar_wait_drain(&sh.do_full[ii % C::NS], (ii / C::NS) & 1, a.timeout_ns);
         }
       }
     } else if (warp == 1) {
@@ -646,16 +543,18 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
         kj = j + 1;
         ok = mbar_wait(&sh.v_empty[vs], ((j / Q::NV) & 1) ^ 1, wc);
         if (!ok) break;
+        vj = j + 1;
+        if (a.fault == 2 && j == 0) continue;  // failure-path test: V_0 never arrives
         mbar_arrive_expect_tx(&sh.v_full[vs], C::TILE_BYTES);
         load_tile<D>(smem + Q::OFF_V + vs * C::TILE_BYTES, &tm_v, &sh.v_full[vs], j * kTileRows, bh);
-        vj = j + 1;
       }
       if (!ok) {
         mbar_wait_drain(&sh.q_full, 0, a.timeout_ns);
         for (int jj = max(0, kj - Q::NK); jj < kj; ++jj)
           mbar_wait_drain(&sh.k_full[jj % Q::NK], (jj / Q::NK) & 1, a.timeout_ns);
         for (int jj = max(0, vj - Q::NV); jj < vj; ++jj)
-          mbar_wait_drain(&sh.v_full[jj % Q::NV], (jj / Q::NV) & 1, a.timeout_ns);
+          if (!(a.fault == 2 && jj == 0))
+            mbar_wait_drain(&sh.v_full[jj % Q::NV], (jj / Q::NV) & 1, a.timeout_ns);
       }
     } else if (warp == 1) {
       // ---------------- tcgen05.mma issuer (the whole warp; one lane issues) ----------------
@@ -805,29 +704,52 @@ __global__ void __launch_bounds__(384, 1)
 // ---------------------------------------------------------------------------
 static int g_num_sms = 0;
 
+static int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_num_sms = n > 0 ? n : 148;
+  }
+  return g_num_sms;
+}
+
+template <int D, bool BF16>
+static cudaError_t launch_bwd_pre_t(const void* o, const void* dO, const float* lse, float* dsum,
+                                    float* l2, float* dq_acc, int BH, int N, int n_pad,
+                                    cudaStream_t stream) {
+  const long long rows = static_cast<long long>(BH) * n_pad;
+  const long long rows_per_block = 8LL * (32 / (D / 8)) * kPrePasses;  // 8 warps
+  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  fa2_bwd_pre_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, dsum, l2, dq_acc, BH,
+      N, n_pad);
+  return cudaGetLastError();
+}
+
+// The preprocessing pass of both backward variants (dq_acc: nullptr, or the
+// fused backward's fp32 dQ accumulator to zero).
+cudaError_t launch_bwd_pre(int d, bool bf16, const void* o, const void* dO, const float* lse,
+                           float* dsum, float* l2, float* dq_acc, int BH, int N, int n_pad,
+                           cudaStream_t stream) {
+  if (d == 64 && bf16) return launch_bwd_pre_t<64, true>(o, dO, lse, dsum, l2, dq_acc, BH, N, n_pad, stream);
+  if (d == 64 && !bf16) return launch_bwd_pre_t<64, false>(o, dO, lse, dsum, l2, dq_acc, BH, N, n_pad, stream);
+  if (d == 128 && bf16) return launch_bwd_pre_t<128, true>(o, dO, lse, dsum, l2, dq_acc, BH, N, n_pad, stream);
+  if (d == 128 && !bf16) return launch_bwd_pre_t<128, false>(o, dO, lse, dsum, l2, dq_acc, BH, N, n_pad, stream);
+  return cudaErrorInvalidValue;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 static cudaError_t launch_bwd_t(const void* o, const void* dO, const float* lse,
                                 const CUtensorMap* maps, const BwdArgs& a, float* dsum,
                                 float* l2, cudaStream_t stream, cudaEvent_t* ev) {
   using C = BwdCfg<D>;
   const int BH = a.B * a.H;
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
   if (ev) cudaEventRecord(ev[0], stream);
   {
-    const long long rows = static_cast<long long>(BH) * a.n_pad;
-    const long long rows_per_block = 8LL * (32 / (D / 8)) * kPrePasses;  // 8 warps
-    long long blocks = (rows + rows_per_block - 1) / rows_per_block;
-    const long long cap = static_cast<long long>(g_num_sms) * 8;
-    if (blocks > cap) blocks = cap;
-    fa2_bwd_pre_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, stream>>>(
-        static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, dsum, l2, BH,
-        a.N, a.n_pad);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_bwd_pre(D, BF16, o, dO, lse, dsum, l2, nullptr, BH, a.N, a.n_pad, stream);
     if (e != cudaSuccess) return e;
   }
   if (ev) cudaEventRecord(ev[1], stream);

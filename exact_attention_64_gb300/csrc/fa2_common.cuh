@@ -68,28 +68,6 @@ __host__ __device__ inline int fwd_block_tiles(int m, int N, int N_k, int causal
   return fwd_kv_tile_end(r0, min(N, r0 + kFwdRowsPerCta), N_k, causal);
 }
 
-// The split count: for each candidate s in [1, min(max_splits, num_sms,
-// num_n_blocks)], the SM utilisation is w / ceil(w) with w = workers * s /
-// num_sms waves (the filled fraction of the waves; the page does not define
-// it); take the best and return the smallest s within 0.95 of it.
-inline int fwd_num_splits(int workers, int num_sms, int num_n_blocks, int max_splits) {
-  int top = max_splits < num_sms ? max_splits : num_sms;
-  if (num_n_blocks < top) top = num_n_blocks;
-  if (top < 1) top = 1;
-  double best = 0.0;
-  for (int s = 1; s <= top; ++s) {
-    const long long cells = static_cast<long long>(workers) * s;
-    const double eff = (static_cast<double>(cells) / num_sms) / static_cast<double>((cells + num_sms - 1) / num_sms);
-    if (eff > best) best = eff;
-  }
-  for (int s = 1; s <= top; ++s) {
-    const long long cells = static_cast<long long>(workers) * s;
-    const double eff = (static_cast<double>(cells) / num_sms) / static_cast<double>((cells + num_sms - 1) / num_sms);
-    if (eff >= 0.95 * best) return s;
-  }
-  return 1;
-}
-
 // Backward work mapping. dK and dV accumulate along the query direction, so
 // their worker owns a K/V column block ("FlashAttention学习笔记(2)",
 // Foward和backward中的thread block划分): one CTA per 128-key block, the column
@@ -152,6 +130,9 @@ struct BwdArgs {
   float scale_log2;       // scale * log2(e)
   int* status;
   unsigned long long timeout_ns;
+  int fault;              // 0 normally; failure-path tests: 1 = the dK/dV workers' producer
+                          // skips the first dO tile, 2 = the dQ workers' producer skips the
+                          // first V tile
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

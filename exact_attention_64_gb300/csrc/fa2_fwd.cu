@@ -74,10 +74,12 @@ struct FwdShared {
 // / l_s and lse_s = m_s + ln l_s (-inf: no key of the part is visible); then
 //   L = ln sum_s exp(lse_s),   O = sum_s exp(lse_s - L) O_s,
 // with O rounded once to the 16-bit type. Each warp merges its 32 rows: lane =
-// row forms L and the weights (staged in the warp's 4 KiB shared slice, 32
-// parts at a time, XOR-swizzled), then the lanes cover 4 rows x 32 columns per
-// load so that every read of the parts is a whole 128-byte segment. The parts
-// were written by other CTAs: they are read through L2 (ld.global.cg).
+// row reads its row's logsumexps (32 parts per batch of loads, all in flight
+// together), forms L with a running max, and stages the weights in the warp's
+// 4 KiB shared slice (XOR-swizzled); then the lanes cover 4 rows x 64 columns
+// per part so that every read of the parts is a whole 128-byte segment and 16
+// reads are in flight per lane and part. The parts were written by other CTAs:
+// they are read through L2 (ld.global.cg).
 template <int D, bool BF16>
 __device__ __forceinline__ void fwd_merge_rows(const FwdArgs& a, int bh, int wrow0, int parts,
                                                int lane, float* wsm) {
@@ -87,38 +89,50 @@ __device__ __forceinline__ void fwd_merge_rows(const FwdArgs& a, int bh, int wro
   const size_t rbase = static_cast<size_t>(bh) * N;
   const int my_row = wrow0 + lane;
   const bool row_in = my_row < N;
-  float mx = -INFINITY;
-  if (row_in)
-    for (int s = 0; s < parts; ++s) mx = fmaxf(mx, __ldcg(a.lse_part + s * bhn + rbase + my_row));
-  float L = -INFINITY;
-  if (mx != -INFINITY) {
-    float tot = 0.f;
-    for (int s = 0; s < parts; ++s)
-      tot += ex2_approx((__ldcg(a.lse_part + s * bhn + rbase + my_row) - mx) * kLog2e);
-    L = mx + lg2_approx(tot) * kLn2;
-  }
-  if (row_in) a.lse[rbase + my_row] = L;
-  // Weights of parts [s0, s0 + 32) of this lane's row: wsm[row][k ^ row].
-  auto stage_weights = [&](int s0) {
-    __syncwarp();
-#pragma unroll 4
-    for (int k = 0; k < 32; ++k) {
-      const int s = s0 + k;
-      float w = 0.f;
-      if (s < parts && L != -INFINITY)
-        w = ex2_approx((__ldcg(a.lse_part + s * bhn + rbase + my_row) - L) * kLog2e);
-      wsm[lane * 32 + (k ^ lane)] = w;
+  // This lane's logsumexps of parts [s0, s0 + 32).
+  auto load_lse = [&](int s0, float (&l)[32]) {
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      l[k] = (row_in && s0 + k < parts) ? __ldcg(a.lse_part + (s0 + k) * bhn + rbase + my_row)
+                                        : -INFINITY;
+  };
+  float lb[32];
+  float mx = -INFINITY, tot = 0.f;
+  for (int s0 = 0; s0 < parts; s0 += 32) {
+    load_lse(s0, lb);
+    float cm = mx;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) cm = fmaxf(cm, lb[k]);
+    if (cm != -INFINITY) {
+      if (mx != -INFINITY) tot *= ex2_approx((mx - cm) * kLog2e);
+#pragma unroll
+      for (int k = 0; k < 32; ++k) tot += ex2_approx((lb[k] - cm) * kLog2e);  // -inf -> 0
+      mx = cm;
     }
+  }
+  const float L = (mx == -INFINITY) ? -INFINITY : mx + lg2_approx(tot) * kLn2;
+  if (row_in) a.lse[rbase + my_row] = L;
+  // Weights of parts [s0, s0 + 32) of this lane's row: wsm[row][k ^ row]. With
+  // at most 32 parts the logsumexps are still in registers.
+  auto stage_weights = [&](int s0) {
+    if (parts > 32) load_lse(s0, lb);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      wsm[lane * 32 + (k ^ lane)] = (L == -INFINITY) ? 0.f : ex2_approx((lb[k] - L) * kLog2e);
     __syncwarp();
   };
   const int sub = lane >> 3, seg = lane & 7;
   const bool once = parts <= 32;
   if (once) stage_weights(0);
+  constexpr int CW = D < 64 ? D : 64;  // columns per pass
 #pragma unroll 1
-  for (int c = 0; c < D; c += 32) {
-    float4 acc[8];
+  for (int c = 0; c < D; c += CW) {
+    float4 acc[CW / 32][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int h = 0; h < CW / 32; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[h][i] = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s0 = 0; s0 < parts; s0 += 32) {
       if (!once) stage_weights(s0);
       const int cnt = min(32, parts - s0);
@@ -130,23 +144,30 @@ __device__ __forceinline__ void fwd_merge_rows(const FwdArgs& a, int bh, int wro
           const int rr = 4 * i + sub;
           if (wrow0 + rr < N) {
             const float w = wsm[rr * 32 + (k ^ rr)];
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(wrow0 + rr) * D));
-            acc[i].x = fmaf(w, x.x, acc[i].x);
-            acc[i].y = fmaf(w, x.y, acc[i].y);
-            acc[i].z = fmaf(w, x.z, acc[i].z);
-            acc[i].w = fmaf(w, x.w, acc[i].w);
+#pragma unroll
+            for (int h = 0; h < CW / 32; ++h) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(
+                  src + static_cast<size_t>(wrow0 + rr) * D + 32 * h));
+              acc[h][i].x = fmaf(w, x.x, acc[h][i].x);
+              acc[h][i].y = fmaf(w, x.y, acc[h][i].y);
+              acc[h][i].z = fmaf(w, x.z, acc[h][i].z);
+              acc[h][i].w = fmaf(w, x.w, acc[h][i].w);
+            }
           }
         }
       }
     }
     uint16_t* o16 = static_cast<uint16_t*>(a.o);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int rr = 4 * i + sub;
-      if (wrow0 + rr < N)
-        *reinterpret_cast<uint2*>(o16 + (rbase + wrow0 + rr) * D + c + seg * 4) =
-            make_uint2(pack_x2<BF16>(acc[i].x, acc[i].y), pack_x2<BF16>(acc[i].z, acc[i].w));
-    }
+    for (int h = 0; h < CW / 32; ++h)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + sub;
+        if (wrow0 + rr < N)
+          *reinterpret_cast<uint2*>(o16 + (rbase + wrow0 + rr) * D + c + 32 * h + seg * 4) =
+              make_uint2(pack_x2<BF16>(acc[h][i].x, acc[h][i].y),
+                         pack_x2<BF16>(acc[h][i].z, acc[h][i].w));
+      }
   }
 }
 
@@ -493,7 +514,7 @@ __global__ void __launch_bounds__(384, 1)
         // this part skipped every wait, so Q's copy may still be landing there.
         bool q_in = true;
         if (nt == 0 && n_total > 0) q_in = mbar_wait_warp(&sh.q_full, 0, wc);
-        if (q_in)
+        if (q_in && *abort_flag == 0)
           fwd_merge_rows<D, BF16>(a, bh, wrow0, parts, lane,
                                   reinterpret_cast<float*>(smem + C::OFF_Q + t * C::TILE_BYTES + quad * 4096));
       }

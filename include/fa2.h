@@ -157,11 +157,18 @@ size_t fa2_step_host_workspace_size(int B, int H, int N, int d, int heads_per_ch
 size_t fa2_fwd_split_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /* The split count of the same page: for each candidate s in 1 .. min(128,
- * num_sms, ceil(N / 128)), SM utilisation = w / ceil(w) with w = workers * s /
- * num_sms waves and workers = B * H * ceil(N / 256) forward CTAs (the page does
- * not define utilisation; this is the filled fraction of the waves); returns
- * the smallest s whose utilisation is at least 0.95 of the best. Host only.
- * Returns 0 for invalid arguments. */
+ * num_sms, K/V tiles of the longest worker), the SM utilisation of the split
+ * launch; returns the smallest s whose utilisation is at least 0.95 of the
+ * best. The page does not define utilisation; here it is the fraction of the
+ * SMs' time spent on K/V tiles, useful tiles / (num_sms * makespan), when the
+ * launch's CTAs (row blocks of 256 queries longest first, each block's parts
+ * in order, heads fastest) start in launch order on the SM that frees first,
+ * each taking its K/V tiles plus 1 tile of fixed cost, plus 6 more if its row
+ * block is split (partial write and merge) -- costs measured on GB300. 1 when
+ * the unsplit launch already reaches 0.95. To split automatically, a caller
+ * passes this count (with the device's SM count) to fa2_fwd_split; forward()
+ * of the Python binding does so by default. Host only; results are cached
+ * per shape. Returns 0 for invalid arguments. */
 int fa2_num_splits(int B, int H, int N, int d, int causal, int num_sms);
 
 /* Forward with different query and key lengths: q, o [B][H][Nq][d], lse
@@ -192,6 +199,29 @@ int fa2_bwd(const void* q, const void* k, const void* v, const void* o, const fl
             const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d, int causal,
             float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Bytes of device workspace fa2_bwd_atomic needs: fa2_bwd's, then the fp32 dQ
+ * accumulator [B*H][N rounded up to 128][d]. Returns 0 for invalid sizes. */
+size_t fa2_bwd_atomic_workspace_size(int B, int H, int N, int d);
+
+/* The same gradients as fa2_bwd, computed the way the pages' column workers
+ * do it ("FlashAttention学习笔记(2)", Foward和backward中的thread block划分; "大猿
+ * 搬砖简记", V2 backward): one CTA per 128-key column block keeps K_j, V_j in
+ * shared memory and dK_j, dV_j in TMEM while the query tiles stream past, and
+ * adds each dQ_i contribution (dS K, fp32) into an accumulator in global
+ * memory with TMA reduce-adds; the preprocessing pass zeroes the accumulator
+ * and a last pass writes dq = scale * accumulator. Five products per (key
+ * block, query tile) pair, against seven for fa2_bwd, but on GB300 it runs
+ * slower than fa2_bwd (the reduce-adds and the longer per-tile chain of the
+ * compute warps); kept as the measured alternative. The order of the
+ * reduce-adds varies from run to run, so dq is not bit-reproducible (dk and
+ * dv are). Equal query and key lengths.
+ *   workspace : >= fa2_bwd_atomic_workspace_size(B,H,N,d) bytes, 256-byte aligned.
+ *   other arguments as in fa2_bwd. */
+int fa2_bwd_atomic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                   const void* dO, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                   void* stream);
+
 /* Backward with different query and key lengths (mask as in fa2_fwd_qk): q, o,
  * dO, dq [B][H][Nq][d], lse [B][H][Nq]; k, v, dk, dv [B][H][Nk][d]. Keys that
  * no query sees (causal, Nk > Nq) get dk = dv = 0. The workspace is
@@ -210,6 +240,14 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
                   int causal, float scale, int dtype, void* workspace, size_t workspace_bytes,
                   void* const* phase_events, void* stream);
 
+/* fa2_bwd_atomic with the same four phase events: before the preprocessing
+ * kernel, between it and the column workers' launch, between that and the dq
+ * conversion, and after it. */
+int fa2_bwd_atomic_timed(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dO, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, int causal, float scale, int dtype, void* workspace,
+                         size_t workspace_bytes, void* const* phase_events, void* stream);
+
 /* fa2_bwd without a caller-provided workspace, for callers that must not
  * allocate device memory: code running inside a memory pool or a framework
  * allocator it does not own, or a process that fixes its device footprint at
@@ -217,14 +255,18 @@ int fa2_bwd_timed(const void* q, const void* k, const void* v, const void* o, co
  * have no counterpart to this entry point; it is a property of this library.)
  * The backward's scratch -- the row sums D and L*log2(e), 8 bytes per query
  * row with rows padded to 128 per head -- lives in a 16 MiB array built into
- * the library, one per GPU that loads it, held until the process exits.
+ * the library, one per GPU that loads it, held until the process exits. Its
+ * gradients are the bits of fa2_bwd on the same inputs.
  *   arguments  : as fa2_bwd, minus the workspace.
  *   limit      : fa2_bwd_workspace_size(B,H,N,d) <= 16 MiB (for example up to
  *                B*H = 256 heads of N = 8192); larger sizes return
  *                FA2_ERR_UNSUPPORTED and touch nothing.
  *   set-up     : the first call on a device looks up the array's device
- *                address with that device current; make that first call
- *                before any stream capture.
+ *                address with that device current and keeps it for the life
+ *                of the process; make that first call before any stream
+ *                capture. A device reset (cudaDeviceReset) reloads the
+ *                library's device code at a new address, so do not use this
+ *                entry point (or the library's status word) across a reset.
  *   concurrency: every call on a device shares the one array, so calls that
  *                may overlap on the GPU (different streams, or different host
  *                threads) race on it; serialise them. Nothing needs clearing
@@ -277,12 +319,20 @@ int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, f
  * or 0. */
 int fa2_last_cuda_error(void);
 
-/* Arms a host-side fault for the NEXT fa2_fwd / fa2_fwd_instrumented call on
- * this process: kind 1 = the producer warp never loads the first V tile, so the
- * MMA warp's wait on it runs out after timeout_ms (1..5000) milliseconds
- * instead of the default 2 s; the kernel then records FA2_ERR_DEVICE_TIMEOUT
- * and returns. kind 0 disarms. Exists to test the failure path without
- * hanging or faulting the GPU. */
+/* Arms a host-side fault for the next call of its kind in this process. Each
+ * kind makes one TMA producer warp skip one load, so that a consumer's bounded
+ * wait on it runs out after timeout_ms (1..5000) milliseconds instead of the
+ * default 2 s; the kernel then records FA2_ERR_DEVICE_TIMEOUT, lets the copies
+ * and MMAs it issued finish, frees its tensor memory and returns:
+ *   1  the next fa2_fwd / fa2_fwd_qk / fa2_fwd_instrumented: the first V tile;
+ *   2  the next fa2_fwd_split: the first V tile of every part;
+ *   3  the next backward (fa2_bwd, fa2_bwd_atomic and their variants): the
+ *      first dO tile of every K/V column worker;
+ *   4  the next fa2_bwd (or fa2_bwd_qk, fa2_bwd_noalloc): the first V tile of
+ *      every dQ worker;
+ *   0  disarms.
+ * Outputs of the faulted call are undefined. Exists to test the failure path
+ * without hanging or faulting the GPU. */
 int fa2_debug_arm_fault(int kind, int timeout_ms);
 
 #ifdef __cplusplus

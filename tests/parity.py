@@ -45,3 +45,9 @@ def rel_fro(a: np.ndarray, ref: np.ndarray) -> float:
     den = float(np.linalg.norm(ref))
     num = float(np.linalg.norm(a - ref))
     return num / den if den > 0 else num
+
+
+def seeded_heads(w, count: int, seed: int):
+    """``count`` distinct (b, h) heads of workload ``w`` drawn by a seeded RNG."""
+    flat = np.random.default_rng(seed).choice(w.B * w.H, size=count, replace=False)
+    return sorted((int(x) // w.H, int(x) % w.H) for x in flat)

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from exact_attention_64_gb300.workloads import WORKLOADS, make_inputs, workload_inputs
-from tests.parity import TOL, oracle_bwd, rel_fro, to64
+from tests.parity import TOL, oracle_bwd, rel_fro, seeded_heads, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -65,16 +65,30 @@ def test_bwd_small_workloads_full(cuda_device, fa2_lib, name):
 
 
 @pytest.mark.parametrize("name", ["bf16_b8h16_n2048_d128", "causal_bf16_b8h16_n2048_d128",
-                                  "causal_bf16_b1h2_n16384_d128",
-                                  "causal_bf16_b4h32_n8192_d128_qstd3"])
-def test_bwd_full_size_sampled_heads(cuda_device, fa2_lib, name):
-    """Full-size launch; whole heads chosen by a seeded draw go through the oracle."""
+                                  "causal_bf16_b1h2_n16384_d128"])
+def test_bwd_full_size_every_head(cuda_device, fa2_lib, name):
+    """Full-size launch; every head's dQ, dK, dV go through the oracle."""
     w = WORKLOADS[name]
     q, k, v, do = workload_inputs(w)
     o, lse, dq, dk, dv = _run(fa2_lib, cuda_device, q, k, v, do, w.causal, w.scale)
-    rng = np.random.default_rng(2)
-    nheads = 1 if w.N >= 8192 else 2
-    heads = sorted({(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(nheads)})
+    tol = TOL[w.torch_dtype]
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            ref = oracle_bwd(q[sl], k[sl], v[sl], do[sl], w.causal, w.scale)
+            _check_grads((dq[sl], dk[sl], dv[sl]), ref, tol)
+
+
+def test_bwd_headline_eight_seeded_heads(cuda_device, fa2_lib):
+    """The 128-head long-sequence workload at full size; eight whole heads
+    drawn by a seeded RNG go through the oracle, and every head's gradients are
+    finite."""
+    w = WORKLOADS["causal_bf16_b4h32_n8192_d128_qstd3"]
+    q, k, v, do = workload_inputs(w)
+    o, lse, dq, dk, dv = _run(fa2_lib, cuda_device, q, k, v, do, w.causal, w.scale)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t).all()
+    heads = seeded_heads(w, 8, 2)
     refs = oracle_bwd(q, k, v, do, w.causal, w.scale, heads=heads)
     tol = TOL[w.torch_dtype]
     for (b, h), (dq_r, dk_r, dv_r) in zip(heads, refs):
@@ -82,18 +96,15 @@ def test_bwd_full_size_sampled_heads(cuda_device, fa2_lib, name):
                      (dq_r, dk_r, dv_r), tol)
 
 
-def test_bwd_invariants_full_size(cuda_device, fa2_lib):
-    """Properties that hold at any size, on every head of a full-size run:
-    rows of P sum to 1 => sum_j dV_j = sum_i dO_i; rows of dS sum to 0 =>
-    sum_j dK_j = 0."""
+def test_bwd_column_sums_of_dv(cuda_device, fa2_lib):
+    """Rows of P sum to 1, so sum_j dV_j = sum_i dO_i for every head (a property
+    of the whole head that element parity checks only term by term)."""
     w = WORKLOADS["causal_bf16_b8h16_n2048_d128"]
     q, k, v, do = workload_inputs(w)
     o, lse, dq, dk, dv = _run(fa2_lib, cuda_device, q, k, v, do, w.causal, w.scale)
     sdv = to64(dv).sum(axis=2)
     sdo = to64(do).sum(axis=2)
     assert np.max(np.abs(sdv - sdo)) / np.max(np.abs(sdo)) <= 2e-2
-    sdk = to64(dk).sum(axis=2)
-    assert np.max(np.abs(sdk)) <= 2e-2 * np.max(np.abs(to64(dk))) * math.sqrt(w.N)
 
 
 def test_bwd_dq_is_deterministic(cuda_device, fa2_lib):
@@ -103,6 +114,39 @@ def test_bwd_dq_is_deterministic(cuda_device, fa2_lib):
     r2 = _run(fa2_lib, cuda_device, q, k, v, do, True, 128 ** -0.5)
     for a, b in zip(r1[2:], r2[2:]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("B,H,N,d,dtype,causal", EDGE[::2] + [(2, 2, 640, 128, torch.bfloat16, True)])
+def test_bwd_atomic_edge_shapes(cuda_device, fa2_lib, B, H, N, d, dtype, causal):
+    """fa2_bwd_atomic (column workers, dQ by fp32 reduce-adds) against the oracle."""
+    q, k, v, do = make_inputs(B, H, N, d, dtype, seed=7 * N + d + 1)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd, dod = (t.to(cuda_device) for t in (q, k, v, do))
+    o, lse = fa2_lib.forward(qd, kd, vd, causal=causal, scale=scale)
+    grads = fa2_lib.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale, atomic=True)
+    torch.cuda.synchronize()
+    assert fa2_lib.device_status() == 0
+    _check_grads([g.cpu() for g in grads], oracle_bwd(q, k, v, do, causal, scale), TOL[dtype])
+
+
+def test_bwd_atomic_headline_two_seeded_heads(cuda_device, fa2_lib):
+    """fa2_bwd_atomic on the 128-head long-sequence workload at full size; two
+    seeded heads through the oracle; its dK and dV are bit-reproducible (only
+    dQ goes through reduce-adds)."""
+    w = WORKLOADS["causal_bf16_b4h32_n8192_d128_qstd3"]
+    q, k, v, do = workload_inputs(w)
+    qd, kd, vd, dod = (t.to(cuda_device) for t in (q, k, v, do))
+    o, lse = fa2_lib.forward(qd, kd, vd, causal=True, scale=w.scale)
+    g1 = [t.clone() for t in fa2_lib.backward(qd, kd, vd, o, lse, dod, causal=True, scale=w.scale,
+                                              atomic=True)]
+    g2 = fa2_lib.backward(qd, kd, vd, o, lse, dod, causal=True, scale=w.scale, atomic=True)
+    torch.cuda.synchronize()
+    assert fa2_lib.device_status() == 0
+    assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
+    heads = seeded_heads(w, 2, 3)
+    refs = oracle_bwd(q, k, v, do, True, w.scale, heads=heads)
+    for (b, h), ref in zip(heads, refs):
+        _check_grads([t[b:b + 1, h:h + 1].cpu() for t in g1], ref, TOL[w.torch_dtype])
 
 
 def test_autograd_function(cuda_device, fa2_lib):

@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from exact_attention_64_gb300.workloads import WORKLOADS, make_inputs, workload_inputs
-from tests.parity import TOL, max_abs, oracle_fwd, to64
+from tests.parity import TOL, max_abs, oracle_fwd, seeded_heads, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -60,21 +60,41 @@ def test_fwd_small_workloads_full(cuda_device, fa2_lib, name):
     assert max_abs(to64(lse), lse_ref) <= tol["lse"]
 
 
-@pytest.mark.parametrize("name", ["bf16_b8h16_n2048_d128", "causal_bf16_b8h16_n2048_d128",
-                                  "causal_bf16_b1h2_n16384_d128",
-                                  "causal_bf16_b4h32_n8192_d128_qstd3"])
-def test_fwd_full_size_sampled_heads(cuda_device, fa2_lib, name):
-    """Full-size launch; the oracle checks whole heads chosen by a seeded draw."""
+@pytest.mark.parametrize("name,num_splits", [("bf16_b8h16_n2048_d128", 1),
+                                             ("causal_bf16_b8h16_n2048_d128", 1),
+                                             ("causal_bf16_b1h2_n16384_d128", 1),
+                                             ("causal_bf16_b1h2_n16384_d128", "auto")])
+def test_fwd_full_size_every_head(cuda_device, fa2_lib, name, num_splits):
+    """Full-size launch; every head goes through the oracle (the two-head long
+    sequence both unsplit and with the library's own K/V split choice)."""
     w = WORKLOADS[name]
     q, k, v, _ = workload_inputs(w)
+    o, lse = fa2_lib.forward(q.to(cuda_device), k.to(cuda_device), v.to(cuda_device),
+                             causal=w.causal, scale=w.scale, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert fa2_lib.device_status() == 0
+    o_ref, lse_ref = oracle_fwd(q, k, v, w.causal, w.scale)
+    tol = TOL[w.torch_dtype]
+    o64, l64 = to64(o.cpu()), to64(lse.cpu())
+    assert np.all(np.isfinite(o64)) and np.all(np.isfinite(l64))
+    for b in range(w.B):
+        for h in range(w.H):
+            assert max_abs(o64[b, h], o_ref[b, h]) <= tol["o"], (b, h)
+            assert max_abs(l64[b, h], lse_ref[b, h]) <= tol["lse"], (b, h)
+
+
+def test_fwd_headline_eight_seeded_heads(cuda_device, fa2_lib):
+    """The 128-head long-sequence workload at full size; eight whole heads
+    drawn by a seeded RNG go through the oracle, and every head's outputs are
+    finite."""
+    w = WORKLOADS["causal_bf16_b4h32_n8192_d128_qstd3"]
+    q, k, v, _ = workload_inputs(w)
     o, lse = _run(fa2_lib, cuda_device, q, k, v, w.causal, w.scale)
-    rng = np.random.default_rng(1)
-    nheads = 2 if w.N >= 8192 else 3
-    heads = sorted({(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(nheads)})
+    heads = seeded_heads(w, 8, 1)
     refs = oracle_fwd(q, k, v, w.causal, w.scale, heads=heads)
     tol = TOL[w.torch_dtype]
     o64, l64 = to64(o), to64(lse)
-    assert np.all(np.isfinite(l64))
+    assert np.all(np.isfinite(o64)) and np.all(np.isfinite(l64))
     for (b, h), (o_ref, lse_ref) in zip(heads, refs):
         assert max_abs(o64[b, h], o_ref[0, 0]) <= tol["o"], (b, h)
         assert max_abs(l64[b, h], lse_ref[0, 0]) <= tol["lse"], (b, h)

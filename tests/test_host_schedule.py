@@ -46,17 +46,32 @@ def test_bwd_block_work_matches_oracle(fa2_lib, N, d, causal):
         assert (i0, i1) == schedule.bwd_q_tile_range(bx, N, qrows, keys, causal)
 
 
+def _block_tiles(N, causal):
+    """K/V tiles of every 256-row forward worker in launch order (causal:
+    longest first), from the oracle's brute-force tile ranges."""
+    nm = schedule.ceil_div(N, 256)
+    order = range(nm - 1, -1, -1) if causal else range(nm)
+    return [schedule.fwd_kv_tile_range(m, N, 256, 128, causal)[1] for m in order]
+
+
 @pytest.mark.parametrize("B,H,N", [(1, 1, 1), (1, 2, 16384), (4, 32, 8192), (2, 3, 1000),
-                                   (1, 1, 100000), (8, 16, 2048), (1, 5, 4096)])
-@pytest.mark.parametrize("num_sms", [1, 132, 148, 152, 160])
+                                   (1, 1, 100000), (8, 16, 2048), (1, 5, 4096), (1, 4, 8192),
+                                   (2, 4, 1024)])
+@pytest.mark.parametrize("num_sms", [1, 132, 152, 160])
 def test_num_splits_matches_oracle(fa2_lib, B, H, N, num_sms):
-    """The library's K/V split count equals the oracle's rule (same workers:
-    one forward CTA per 256 query rows; same tiles of 128 keys)."""
+    """The library's K/V split count equals the oracle's rule (makespan
+    utilisation of the same launch: one forward CTA per 256 query rows, 128
+    keys per tile, row blocks longest first under the causal mask)."""
     lib = fa2_lib.load_library()
-    workers = B * H * schedule.ceil_div(N, 256)
-    want = schedule.num_splits_heuristic(workers, num_sms, schedule.ceil_div(N, 128), 128)
     for causal in (0, 1):
-        assert lib.fa2_num_splits(B, H, N, 128, causal, num_sms) == want
+        want = schedule.num_splits_makespan(_block_tiles(N, causal), B * H, num_sms, 128)
+        assert lib.fa2_num_splits(B, H, N, 128, causal, num_sms) == want, causal
+
+
+def test_num_splits_of_the_two_head_long_sequence(fa2_lib):
+    """B=1 H=2 N=16384 causal on GB300's 152 SMs: 4 parts (the fastest split
+    count measured on that shape)."""
+    assert fa2_lib.load_library().fa2_num_splits(1, 2, 16384, 128, 1, 152) == 4
 
 
 def test_num_splits_rejects_bad_arguments(fa2_lib):
