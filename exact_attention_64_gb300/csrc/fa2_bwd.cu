@@ -50,10 +50,13 @@ struct BwdCfg {
   static constexpr int THREADS = 384;
   static constexpr uint32_t TMEM_COLS = 512;
   // dK/dV worker TMEM: dV, dK accumulators, S^T and dP^T. A warpgroup owns 64
-  // query columns of each region; once it has read dP^T for 32 of its queries
-  // (half h), it writes those 32 columns back as 16 columns of P^T and 16 of
-  // dS^T (16-bit pairs): [P^T h0 | dS^T h0 | P^T h1 | dS^T h1].
+  // query columns of each region. Once it has read its S^T columns it writes
+  // P^T over the first 32 of them (16-bit pairs, query 2c and 2c+1 in column
+  // c), and once it has read its dP^T columns it writes dS^T over the first 32
+  // of those, so the A operand of dV (dK) for 16-query block kk sits at column
+  // KV_ST (KV_DPT) + 64 * (kk / 4) + 8 * (kk % 4).
   static constexpr uint32_t KV_DV = 0, KV_DK = D, KV_ST = 2 * D, KV_DPT = 2 * D + 128;
+  __host__ __device__ static constexpr uint32_t pair_col(int kk) { return 64u * (kk / 4) + 8u * (kk % 4); }
   // dQ worker TMEM: S, dP, the dQ accumulator and two dS buffers.
   static constexpr uint32_t Q_S = 0, Q_DP = 128, Q_DQ = 256;
   __host__ __device__ static constexpr uint32_t Q_DS(int b) { return 256 + D + 64 * b; }
@@ -63,11 +66,11 @@ struct BwdKvShared {
   uint64_t kv_full;
   uint64_t q_full[2], do_full[2];  // streamed pair ring: Q_i and dO_i landed (separately, so
   uint64_t s_empty[2];             // S^T(i) need not wait for dO_i); both free again
-  uint64_t st_full, st_free;       // S^T(i) complete / read into registers by all 8 compute warps
+  uint64_t st_full;                // S^T(i) complete
   uint64_t dpt_full;               // dP^T(i) complete
-  uint64_t pds_done[2];            // P^T(i), dS^T(i) of query half h written by all 8 warps
-  uint64_t gr_done;                // dV(i), dK(i) complete: the dP^T region is free
-  uint64_t mma_done;               // one arrival from each of the two MMA issuers
+  uint64_t p_done;                 // P^T(i) written over S^T(i) by all 8 compute warps
+  uint64_t ds_done;                // dS^T(i) written over dP^T(i) by all 8 compute warps
+  uint64_t mma_done;               // every product of the block has completed
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -179,14 +182,17 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // 2. dK / dV workers (K/V outer, Q inner)
 // ---------------------------------------------------------------------------
-// Warp roles: warp 0 TMA; warp 1 issues the score products S^T(i), dP^T(i);
-// warp 2 issues the gradient products dV(i), dK(i); warps 4-7 and 8-11 compute
-// P^T and dS^T for query columns [0,64) and [64,128) of each tile (TMEM lane =
-// key). The compute warps read all of S^T(i) into registers first, which frees
-// its TMEM region for S^T(i+1) at once; P^T(i) and dS^T(i) then go into the
-// dP^T region after dP^T(i) has been read. The exponentials of P^T(i) thus
-// overlap dV/dK(i-1) and dP^T(i) on the tensor core, and the only chain from
-// one tile to the next is dP^T -> dS^T -> dV, dK -> dP^T.
+// Warp roles: warp 0 TMA; warp 1 issues every product; warps 4-7 and 8-11
+// compute P^T and dS^T for query columns [0,64) and [64,128) of each tile
+// (TMEM lane = key). P^T(i) replaces S^T(i) in TMEM as soon as it is formed,
+// so dV(i) runs before dS^T(i) exists, and dS^T(i) replaces dP^T(i). The
+// tensor core runs
+//   ... dV(i), S^T(i+1), dK(i), dP^T(i+1), dV(i+1) ...
+// in issue order, which also orders each product that overwrites a TMEM region
+// after the product that reads it. Two chains cross from tile to tile:
+// S^T -> P^T -> dV -> S^T and dP^T -> dS^T -> dK -> dP^T; each holds two
+// products and one step of the compute warps, so while the compute warps form
+// P^T(i+1) the tensor core runs dK(i) and dP^T(i+1).
 // One dK/dV worker (key block nb of batch*head bh), run by a CTA of the
 // backward's main launch.
 template <int D, bool BF16, bool CAUSAL>
@@ -216,12 +222,10 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
       mbar_init(&sh.s_empty[s], 1);
     }
     mbar_init(&sh.st_full, 1);
-    mbar_init(&sh.st_free, 8);  // the eight compute warps
     mbar_init(&sh.dpt_full, 1);
-    mbar_init(&sh.pds_done[0], 8);
-    mbar_init(&sh.pds_done[1], 8);
-    mbar_init(&sh.gr_done, 1);
-    mbar_init(&sh.mma_done, 2);
+    mbar_init(&sh.p_done, 8);  // the eight compute warps
+    mbar_init(&sh.ds_done, 8);
+    mbar_init(&sh.mma_done, 1);
     sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -269,74 +273,54 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
         }
       }
     } else if (warp == 1) {
-      // ---------------- tcgen05.mma issuer 1 (whole warp, one lane issues): score products ----------------
-      // dP^T(i) overwrites the region that holds P^T/dS^T(i-1), so it waits for
-      // dV/dK(i-1); it is issued before S^T(i+1), which only needs the compute
-      // warps to have read S^T(i) (st_free), so the tile-to-tile chain is not
-      // held up behind the next tile's scores.
+      // ---------------- tcgen05.mma issuer (whole warp, one lane issues) ----------------
       const uint32_t k_s = smem_u32(smem + C::OFF_FIX0), v_s = smem_u32(smem + C::OFF_FIX1);
       auto q_at = [&](int i) { return smem_u32(smem + C::OFF_STR0 + (i % C::NS) * C::TILE_BYTES); };
       auto do_at = [&](int i) { return smem_u32(smem + C::OFF_STR1 + (i % C::NS) * C::TILE_BYTES); };
+      const uint32_t t_pt = tmem + C::KV_ST, t_dst = tmem + C::KV_DPT;
+      auto pt_col = [t_pt](int kk) { return t_pt + C::pair_col(kk); };
+      auto dst_col = [t_dst](int kk) { return t_dst + C::pair_col(kk); };
       bool ok = n_steps == 0 ||
                 (mbar_wait_warp(&sh.kv_full, 0, wc) && mbar_wait_warp(&sh.q_full[0], 0, wc));
       if (ok && n_steps > 0) {
         tc_fence_after();
         mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(0));
         umma_commit_warp(&sh.st_full);
+        ok = mbar_wait_warp(&sh.do_full[0], 0, wc);
+        if (ok) {
+          tc_fence_after();
+          mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_at(0));
+          umma_commit_warp(&sh.dpt_full);
+        }
       }
       for (int i = 0; i < n_steps && ok; ++i) {
-        ok = (i == 0) ? mbar_wait_warp(&sh.do_full[0], 0, wc)
-                      : mbar_wait2_warp(&sh.do_full[i % C::NS], (i / C::NS) & 1, &sh.gr_done,
-                                        (i - 1) & 1, wc);
+        const int nx = i + 1;
+        // dV += P^T(i) dO_i, then S^T(i+1) over the region P^T(i) is read from.
+        ok = mbar_wait_warp(&sh.p_done, i & 1, wc);
         if (!ok) break;
         tc_fence_after();
-        mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_at(i));
-        umma_commit_warp(&sh.dpt_full);
-        if (i + 1 < n_steps) {
-          ok = mbar_wait2_warp(&sh.q_full[(i + 1) % C::NS], ((i + 1) / C::NS) & 1, &sh.st_free,
-                               i & 1, wc);
+        mma_tmem_x_tile<D, BF16>(tmem + C::KV_DV, pt_col, do_at(i), i > 0);
+        if (nx < n_steps) {
+          ok = mbar_wait_warp(&sh.q_full[nx % C::NS], (nx / C::NS) & 1, wc);
           if (!ok) break;
           tc_fence_after();
-          mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(i + 1));
+          mma_rows_x_rows<D, BF16>(tmem + C::KV_ST, k_s, q_at(nx));
           umma_commit_warp(&sh.st_full);
         }
-      }
-      umma_commit_warp(&sh.mma_done);
-      mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
-    } else if (warp == 2) {
-      // ---------------- tcgen05.mma issuer 2 (whole warp, one lane issues): gradient products ----------------
-      // dV += P^T dO_i and dK += dS^T Q_i, in two steps: the 16-query blocks of
-      // query half h of both warpgroups as soon as all eight compute warps have
-      // written that half. S^T(i) and dP^T(i) completed before that, so the
-      // commit after dK(i) also releases the tile's Q/dO stage.
-      constexpr uint32_t idesc = make_idesc_f16(128, D, BF16, false, true);
-      bool ok = true;
-      const uint32_t t_g = tmem + C::KV_DPT;
-      for (int i = 0; i < n_steps && ok; ++i) {
-        const int st = i % C::NS;
-        const uint32_t q_s = smem_u32(smem + C::OFF_STR0 + st * C::TILE_BYTES);
-        const uint32_t do_s = smem_u32(smem + C::OFF_STR1 + st * C::TILE_BYTES);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          ok = mbar_wait_warp(&sh.pds_done[h], i & 1, wc);
+        // dK += dS^T(i) Q_i, then dP^T(i+1) over the region dS^T(i) is read
+        // from. dK(i) is the last reader of Q_i and dO_i: its commit frees the stage.
+        ok = mbar_wait_warp(&sh.ds_done, i & 1, wc);
+        if (!ok) break;
+        tc_fence_after();
+        mma_tmem_x_tile<D, BF16>(tmem + C::KV_DK, dst_col, q_at(i), i > 0);
+        umma_commit_warp(&sh.s_empty[i % C::NS]);
+        if (nx < n_steps) {
+          ok = mbar_wait_warp(&sh.do_full[nx % C::NS], (nx / C::NS) & 1, wc);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll
-          for (int w = 0; w < 2; ++w)
-#pragma unroll
-            for (int sub = 0; sub < 2; ++sub) {
-              const int kk = 4 * w + 2 * h + sub;  // 16-query block of the tile
-              const uint32_t acc = (i > 0 || h > 0 || w > 0 || sub > 0) ? 1u : 0u;
-              const uint32_t col = t_g + 64 * w + 32 * h + 8 * sub;
-              umma_ts_warp(tmem + C::KV_DV, col,
-                           make_sdesc_sw128(do_s + kk * 2048, C::SLAB_BYTES, 1024), idesc, acc);
-              umma_ts_warp(tmem + C::KV_DK, col + 16,
-                           make_sdesc_sw128(q_s + kk * 2048, C::SLAB_BYTES, 1024), idesc, acc);
-            }
+          mma_rows_x_rows<D, BF16>(tmem + C::KV_DPT, v_s, do_at(nx));
+          umma_commit_warp(&sh.dpt_full);
         }
-        if (!ok) break;
-        umma_commit_warp(&sh.gr_done);
-        umma_commit_warp(&sh.s_empty[st]);
       }
       umma_commit_warp(&sh.mma_done);
       mbar_wait_drain(&sh.mma_done, 0, a.timeout_ns);
@@ -381,15 +365,12 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
       if (!ok) break;
       __syncwarp();  // the warp-collective TMEM loads below need a converged warp
       tc_fence_after();
-      // All 64 columns of S^T into registers, then release the region for S^T(i+1).
+      // All 64 columns of S^T into registers; P^T then goes over the first 32.
       uint32_t sv[64];
       tmem_ld_32x32b_x32(t_st, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       tmem_ld_32x32b_x32(t_st + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_wait_ld();
       reg_fence(sv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.st_free);
       const bool need_mask = (CAUSAL && qc0 < n0 + kTileRows - 1) || (qc0 + 64 > N) ||
                              (n0 + kTileRows > Nk);
       // P^T as 16-bit pairs; dS^T below is formed from these rounded values.
@@ -405,6 +386,11 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[16 * h + j] = pack_x2<BF16>(p[2 * j], p[2 * j + 1]);
       }
+      tmem_st_32x32b_x32(t_st, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.p_done);
       float dreg[64];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
@@ -416,30 +402,29 @@ __device__ __forceinline__ void bwd_dkdv_cta(const CUtensorMap& tm_q, const CUte
       if (!ok) break;
       __syncwarp();
       tc_fence_after();
+      // dS^T = P^T o (dP^T - D) from the rounded P^T, over the first 32 dP^T
+      // columns once all 64 have been read.
+      uint32_t dsk[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t dp[32];
         tmem_ld_32x32b_x32(t_dpt + 32 * h, dp);
         tmem_wait_ld();
         reg_fence(dp);
-        // These 32 dP^T columns have been read: they now take P^T (16 pairs)
-        // and dS^T = P^T o (dP^T - D) (16 pairs) for queries 32h..32h+31.
-        uint32_t out[32];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int c = 32 * h + 2 * j;
-          out[j] = pk[16 * h + j];
           const float2 ds = f2_mul(unpack_x2<BF16>(pk[16 * h + j]),
                                    f2_sub(make_float2(__uint_as_float(dp[2 * j]), __uint_as_float(dp[2 * j + 1])),
                                           make_float2(dreg[c], dreg[c + 1])));
-          out[16 + j] = pack_x2<BF16>(ds.x, ds.y);
+          dsk[16 * h + j] = pack_x2<BF16>(ds.x, ds.y);
         }
-        tmem_st_32x32b_x32(t_dpt + 32 * h, out);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.pds_done[h]);
       }
+      tmem_st_32x32b_x32(t_dpt, dsk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.ds_done);
     }
     // ---------------- epilogue: dV, scale*dK -> 16-bit, TMA store ----------------
     if (ok) ok = mbar_wait_warp(&sh.mma_done, 0, wc);
