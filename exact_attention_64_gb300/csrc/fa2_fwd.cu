@@ -258,15 +258,17 @@ __global__ void __launch_bounds__(384, 1)
   const int row0 = mb * kFwdRowsPerCta;
   const int rows_a = min(kTileRows, N - row0);
   const int rows_b = max(0, min(kTileRows, N - row0 - kTileRows));
-  const int end_t[2] = {fwd_kv_tile_end(row0, row0 + rows_a, Nk, CAUSAL),
-                        fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, Nk, CAUSAL)};
+  // Per-tile values are kept as scalars: a two-element array indexed by the
+  // warp's tile would live in local memory and be reloaded in the loops.
+  const int end_a = fwd_kv_tile_end(row0, row0 + rows_a, Nk, CAUSAL);
+  const int end_b = fwd_kv_tile_end(row0 + kTileRows, row0 + kTileRows + rows_b, Nk, CAUSAL);
   // This CTA's part [kv_lo, kv_hi) of the block's K/V tiles. Below, j counts
   // tiles within the part (ring slots, phases, first-tile flags); kv_lo + j is
   // the K/V tile itself (TMA coordinates, masks).
   int kv_lo, kv_hi;
-  fwd_part_range(max(end_t[0], end_t[1]), parts, split, &kv_lo, &kv_hi);
-  const int n_t[2] = {max(0, min(kv_hi, end_t[0]) - kv_lo), max(0, min(kv_hi, end_t[1]) - kv_lo)};
-  const int n_total = max(n_t[0], n_t[1]);
+  fwd_part_range(max(end_a, end_b), parts, split, &kv_lo, &kv_hi);
+  const int n_a = max(0, min(kv_hi, end_a) - kv_lo), n_b = max(0, min(kv_hi, end_b) - kv_lo);
+  const int n_total = max(n_a, n_b);
   const uint32_t tmem = sh.tmem_base;
   volatile int* abort_flag = &sh.abort_flag;
   const WaitCtx wc{a.status, abort_flag, a.timeout_ns};
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t k0 = smem_u32(smem + C::OFF_K);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (n_t[t] > 0) {
+          if ((t == 0 ? n_a : n_b) > 0) {
             issue_qk<D, BF16>(tmem + C::TM_S(t), q_s[t], k0);
             umma_commit_warp(&sh.s_full[t]);
           }
@@ -352,13 +354,14 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t k_next = smem_u32(smem + C::OFF_K + ((j + 1) % C::NK) * C::TILE_BYTES);
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j < n_t[t]) {
+          const int n_this = t == 0 ? n_a : n_b;
+          if (j < n_this) {
             ok = mbar_wait_warp(&sh.p_full[t], j & 1, wc);
             if (!ok) break;
             tc_fence_after();
             issue_pv<D, BF16>(tmem + C::TM_O(t), tmem + C::TM_S(t) + C::TM_P_OFF, v_smem, j > 0);
             umma_commit_warp(&sh.o_full[t]);
-            if (j + 1 < n_t[t]) {
+            if (j + 1 < n_this) {
               issue_qk<D, BF16>(tmem + C::TM_S(t), q_s[t], k_next);
               umma_commit_warp(&sh.s_full[t]);
             }
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r = quad * 32 + lane; // row inside the tile == TMEM lane
     const int row_base = row0 + t * kTileRows;
     const int my_row = row_base + r;
-    const int nt = n_t[t];
+    const int nt = t == 0 ? n_a : n_b;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::TM_S(t);
     const uint32_t t_p = t_s + C::TM_P_OFF;
