@@ -211,10 +211,12 @@ def run_reference(args, w, rank, world):
 
 TRAFFIC_FILES = {
     "fa2_fwd_kernel": ["fa2_fwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
-    "fa2_bwd_main_kernel": ["fa2_bwd.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_main_kernel": ["fa2_bwd.cu", "fa2_bwd_persist.cuh", "fa2_bwd_parts.cuh", "fa2_common.cuh",
+                            "sm103_ptx.cuh"],
     "fa2_bwd_fused_kernel": ["fa2_bwd_fused.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh",
                              "sm103_ptx.cuh"],
-    "fa2_bwd_pre_kernel": ["fa2_bwd.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_bwd_pre_kernel": ["fa2_bwd.cu", "fa2_bwd_persist.cuh", "fa2_bwd_parts.cuh", "fa2_common.cuh",
+                           "sm103_ptx.cuh"],
     "fa2_bwd_dq_convert_kernel": ["fa2_bwd_fused.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh",
                                   "sm103_ptx.cuh"],
 }

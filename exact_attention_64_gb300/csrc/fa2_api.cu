@@ -450,11 +450,11 @@ int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, f
 
 size_t fa2_bwd_workspace_size(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
-  // [D: B*H x N_pad fp32][L*log2e: B*H x N_pad fp32], N_pad = N rounded up to
-  // the 128-row tile of the backward kernels.
+  // [D: B*H x N_pad fp32][L*log2e: B*H x N_pad fp32][work counter: 256 bytes],
+  // N_pad = N rounded up to the 128-row tile of the backward kernels.
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t n_pad = align_up(static_cast<size_t>(N), 128);
-  return 2 * align_up(bh * n_pad * 4, 256);
+  return 2 * align_up(bh * n_pad * 4, 256) + 256;
 }
 
 size_t fa2_bwd_atomic_workspace_size(int B, int H, int N, int d) {
@@ -522,7 +522,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   const size_t lbytes_pad = align_up(static_cast<size_t>(BH) * n_pad * 4, 256);
   float* dsum = static_cast<float*>(workspace);
   float* l2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + lbytes_pad);
-  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * lbytes_pad);
+  int* item_counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + 2 * lbytes_pad);
+  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * lbytes_pad + 256);
   if (atomic && make_map_dqacc(&maps[7], dq_acc, BH, static_cast<int>(n_pad), d) != FA2_OK)
     return FA2_ERR_CUDA;
   fa2::BwdArgs a{};
@@ -538,6 +539,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   a.status = status;
   a.timeout_ns = fa2::kDefaultWaitTimeoutNs;
   a.fault = 0;
+  a.item_counter = item_counter;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
   {
     // Kind 3 is consumed by the next backward of either kind: the producer of
     // the K/V column workers skips the first dO tile. Kind 4 by the next

@@ -450,8 +450,8 @@ __global__ void __launch_bounds__(256)
 // Host-side launcher
 // ---------------------------------------------------------------------------
 cudaError_t launch_bwd_pre(int d, bool bf16, const void* o, const void* dO, const float* lse,
-                           float* dsum, float* l2, float* dq_acc, int BH, int N, int n_pad,
-                           cudaStream_t stream);
+                           float* dsum, float* l2, float* dq_acc, int* item_counter, int BH, int N,
+                           int n_pad, cudaStream_t stream);
 
 template <int D, bool BF16, bool CAUSAL>
 static cudaError_t launch_bwd_fused_t(const void* o, const void* dO, const float* lse,
@@ -461,7 +461,7 @@ static cudaError_t launch_bwd_fused_t(const void* o, const void* dO, const float
   using C = FusedCfg<D>;
   const int BH = a.B * a.H;
   if (ev) cudaEventRecord(ev[0], stream);
-  cudaError_t e = launch_bwd_pre(D, BF16, o, dO, lse, dsum, l2, dq_acc, BH, a.N, a.n_pad, stream);
+  cudaError_t e = launch_bwd_pre(D, BF16, o, dO, lse, dsum, l2, dq_acc, nullptr, BH, a.N, a.n_pad, stream);
   if (e != cudaSuccess) return e;
   if (ev) cudaEventRecord(ev[1], stream);
   {

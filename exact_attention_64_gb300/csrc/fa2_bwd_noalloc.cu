@@ -1,6 +1,7 @@
 // Backward pass for callers that must not allocate device memory.
 //
-// fa2_bwd needs a small scratch workspace (the row sums D and L * log2(e)).
+// fa2_bwd needs a small scratch workspace (the row sums D and L * log2(e), and
+// the work counter of its persistent main launch).
 // Some callers cannot provide one: code running inside a memory pool they do
 // not own, a plugin of a framework whose allocator must not be bypassed, or a
 // process that has fixed its device footprint in advance and forbids
@@ -15,9 +16,10 @@
 namespace {
 
 // Size of the built-in scratch: D and L*log2e take 8 bytes per query row,
-// rows padded to 128 per head, so 16 MiB serves up to about two million
-// padded rows (for example B*H = 128 heads of 8192 rows, which needs 8 MiB).
-constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+// rows padded to 128 per head, and the work counter 256 bytes, so 16 MiB + 256
+// serves up to about two million padded rows (for example B*H = 256 heads of
+// 8192 rows).
+constexpr size_t kNoAllocScratchBytes = (size_t(16) << 20) + 256;
 constexpr int kMaxDevices = 64;
 
 // One copy per GPU that loads the library, held until the process exits.

@@ -130,9 +130,14 @@ struct BwdArgs {
   float scale_log2;       // scale * log2(e)
   int* status;
   unsigned long long timeout_ns;
-  int fault;              // 0 normally; failure-path tests: 1 = the dK/dV workers' producer
-                          // skips the first dO tile, 2 = the dQ workers' producer skips the
-                          // first V tile
+  int fault;              // 0 normally; failure-path tests: 1 = the producer skips the
+                          // first dO tile of the first dK/dV item, 2 = the first V tile
+                          // of the first dQ item
+  int* item_counter;      // persistent main launch: work items taken so far; the
+                          // preprocessing pass zeroes it
+  void* dq;               // persistent main launch: outputs written from TMEM by row,
+  void* dk;               // [B*H][N][d] (dq) and [B*H][Nk][d] (dk, dv), 16-bit
+  void* dv;
 };
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {

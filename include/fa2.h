@@ -181,7 +181,8 @@ int fa2_fwd_qk(const void* q, const void* k, const void* v, void* o, float* lse,
                int Nq, int Nk, int d, int causal, float scale, int dtype, void* stream);
 
 /* Bytes of device workspace fa2_bwd needs: the fp32 row sums D = rowsum(dO o O)
- * and L * log2(e), each [B*H][N rounded up to 128]. Returns 0 for invalid sizes. */
+ * and L * log2(e), each [B*H][N rounded up to 128], then 256 bytes for the
+ * work counter of the main launch. Returns 0 for invalid sizes. */
 size_t fa2_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass (FlashAttention-2 backward: D = rowsum(dO o O) first; then K/V
@@ -254,11 +255,12 @@ int fa2_bwd_atomic_timed(const void* q, const void* k, const void* v, const void
  * start-up and may not call cudaMalloc afterwards. (The FlashAttention-2 pages
  * have no counterpart to this entry point; it is a property of this library.)
  * The backward's scratch -- the row sums D and L*log2(e), 8 bytes per query
- * row with rows padded to 128 per head -- lives in a 16 MiB array built into
+ * row with rows padded to 128 per head, and a 256-byte work counter -- lives
+ * in a 16 MiB + 256 byte array built into
  * the library, one per GPU that loads it, held until the process exits. Its
  * gradients are the bits of fa2_bwd on the same inputs.
  *   arguments  : as fa2_bwd, minus the workspace.
- *   limit      : fa2_bwd_workspace_size(B,H,N,d) <= 16 MiB (for example up to
+ *   limit      : fa2_bwd_workspace_size(B,H,N,d) <= 16 MiB + 256 (for example up to
  *                B*H = 256 heads of N = 8192); larger sizes return
  *                FA2_ERR_UNSUPPORTED and touch nothing.
  *   set-up     : the first call on a device looks up the array's device

@@ -92,14 +92,15 @@ def test_workspace_size(fa2_lib):
     for fn in (lib.fa2_bwd_workspace_size, lib.fa2_bwd_atomic_workspace_size):
         assert fn(0, 1, 1, 64) == 0
         assert fn(1, 1, 1, 96) == 0
-    # D and L*log2e, each [B*H][N rounded up to 128] fp32
-    assert lib.fa2_bwd_workspace_size(1, 1, 100, 64) == 2 * 512
+    # D and L*log2e, each [B*H][N rounded up to 128] fp32, then 256 bytes for
+    # the persistent main launch's work counter
+    assert lib.fa2_bwd_workspace_size(1, 1, 100, 64) == 2 * 512 + 256
     B, H, N, d = 4, 32, 8192, 128
-    assert lib.fa2_bwd_workspace_size(B, H, N, d) == 2 * B * H * N * 4
+    assert lib.fa2_bwd_workspace_size(B, H, N, d) == 2 * B * H * N * 4 + 256
     # fa2_bwd_atomic: the same, then the fp32 dQ accumulator [B*H][N rounded up to 128][d]
-    assert lib.fa2_bwd_atomic_workspace_size(1, 1, 100, 64) == 2 * 512 + 128 * 64 * 4
-    assert lib.fa2_bwd_atomic_workspace_size(B, H, N, d) == 2 * B * H * N * 4 + B * H * N * d * 4
-    assert lib.fa2_bwd_atomic_workspace_size(3, 1, 129, 128) == 2 * 3 * 256 * 4 + 3 * 256 * 128 * 4
+    assert lib.fa2_bwd_atomic_workspace_size(1, 1, 100, 64) == 2 * 512 + 256 + 128 * 64 * 4
+    assert lib.fa2_bwd_atomic_workspace_size(B, H, N, d) == 2 * B * H * N * 4 + 256 + B * H * N * d * 4
+    assert lib.fa2_bwd_atomic_workspace_size(3, 1, 129, 128) == 2 * 3 * 256 * 4 + 256 + 3 * 256 * 128 * 4
 
 
 def test_fault_arming_validates(fa2_lib):

@@ -64,8 +64,9 @@ def test_noalloc_backward_matches_workspace_backward(cuda_device, fa2_lib):
 
 
 def test_noalloc_size_limit_at_its_boundary(fa2_lib):
-    """The built-in array holds 16 MiB: 8 bytes per padded query row. B*H = 256
-    heads of N = 8192 need exactly 16 MiB and pass the size check (this call
+    """The built-in array holds 16 MiB + 256 bytes: 8 bytes per padded query row
+    and the work counter. B*H = 256 heads of N = 8192 need exactly that and pass
+    the size check (this call
     then fails on its invalid dtype, or on a machine without a GPU on the
     device lookup, but never with FA2_ERR_UNSUPPORTED); 257 heads, or N = 8193
     (one more 128-row tile per head), are refused with FA2_ERR_UNSUPPORTED
@@ -74,7 +75,7 @@ def test_noalloc_size_limit_at_its_boundary(fa2_lib):
     fn = _noalloc(lib)
     a = 0x10000000
     ptrs = [a + i * 0x01000000 for i in range(9)]
-    assert lib.fa2_bwd_workspace_size(16, 16, 8192, 128) == 16 << 20
+    assert lib.fa2_bwd_workspace_size(16, 16, 8192, 128) == (16 << 20) + 256
     bad_dtype = 7
     assert fn(*ptrs, 16, 16, 8192, 128, 1, 0.088, bad_dtype, None) in (FA2_ERR_INVALID_ARG,
                                                                         FA2_ERR_CUDA)
