@@ -40,7 +40,11 @@ struct BwdPShared {
   uint64_t qq_full;                // Q, dO of the item landed
   uint64_t k_full[3], k_empty[3];  // K ring
   uint64_t v_full[2], v_empty[2];  // V ring
-  uint64_t sq_full, sq_free, dsq_full;
+  uint64_t sq_full, sq_free;
+  uint64_t dsq_full[2];            // dS(h) written by the 8 compute warps, one barrier per dS
+                                   // buffer: the warps may finish dS(h+1) before the issuer has
+                                   // waited for dS(h), and a parity wait must never fall two
+                                   // phases behind its barrier
   uint64_t q_res_free;             // the item's last S and dP complete: Q, dO may be replaced
   uint64_t dq_acc_done;            // the item's last dQ product complete
   // items
@@ -343,7 +347,7 @@ __device__ bool bwd_persist_issuer(BwdPShared& sh, uint8_t* smem, uint32_t tmem,
             umma_commit_warp(&sh.v_empty[hx % Q::NV]);
             if (j + 2 == tiles) umma_commit_warp(&sh.q_res_free);
           }
-          ok = mbar_wait_warp(&sh.dsq_full, h & 1, wc);
+          ok = mbar_wait_warp(&sh.dsq_full[h & 1], (h >> 1) & 1, wc);
           if (!ok) break;
           tc_fence_after();
           const uint32_t ds_col = tmem + C::Q_DS(h & 1);
@@ -568,7 +572,7 @@ __device__ bool bwd_persist_compute(BwdPShared& sh, uint8_t* smem, uint32_t tmem
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.dsq_full);
+        if (lane == 0) mbar_arrive(&sh.dsq_full[h & 1]);
       }
       if (!ok) break;
       // Epilogue: scale * dQ of this block's rows; warpgroup w stores columns [w*D/2, (w+1)*D/2).
@@ -626,7 +630,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(&sh.sq_full, 1);
     mbar_init(&sh.sq_free, 8);
-    mbar_init(&sh.dsq_full, 8);
+    mbar_init(&sh.dsq_full[0], 8);
+    mbar_init(&sh.dsq_full[1], 8);
     mbar_init(&sh.q_res_free, 1);
     mbar_init(&sh.dq_acc_done, 1);
     for (int s = 0; s < kItemSlots; ++s) {

@@ -48,3 +48,25 @@ def test_step_host_from_pageable_memory(cuda_device, fa2_lib):
                               causal=True, heads_per_chunk=3, device=cuda_device)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("hpc", [4, 16])
+def test_step_host_repeated_long_sequence_chunks(cuda_device, fa2_lib, hpc):
+    """Repeated steps over 16 causal heads of 8192 rows in chunks of 1 to 16
+    heads: consecutive chunks' backward launches overlap on the two slot
+    streams, and every call ends with a clean device status and the same bits
+    as the first."""
+    q, k, v, do = make_inputs(1, 16, 8192, 128, torch.bfloat16, seed=5)
+    scale = 128 ** -0.5
+    hq, hk, hv, hdo = (t.pin_memory() for t in (q, k, v, do))
+    first = None
+    for _ in range(4):
+        with torch.cuda.device(cuda_device):
+            out = fa2_lib.step_host(hq, hk, hv, hdo, causal=True, scale=scale,
+                                    heads_per_chunk=hpc, device=cuda_device)
+        assert fa2_lib.device_status() == 0
+        if first is None:
+            first = [t.clone() for t in out]
+        else:
+            for a, b in zip(first, out):
+                assert torch.equal(a, b)
