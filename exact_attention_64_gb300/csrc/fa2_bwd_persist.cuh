@@ -1,7 +1,8 @@
 // The backward's main launch (included by fa2_bwd.cu after the shared-memory
 // and TMEM layouts it uses, BwdCfg and DqCfg).
 //
-// One CTA per SM takes work items from a counter in the workspace: first the
+// One CTA per SM takes work items from a counter in the workspace (its first
+// item is its own index): first the
 // dK/dV workers' key blocks ("FlashAttention学习笔记(2)", Foward和backward中的
 // thread block划分: one worker per K/V column block), then the dQ workers'
 // query blocks, each in the order the per-block launch used (block fastest,
@@ -124,7 +125,11 @@ __device__ bool bwd_persist_producer(BwdPShared& sh, uint8_t* smem, const CUtens
       ok = mbar_wait(&sh.item_empty[slot], ((k / kItemSlots) & 1) ^ 1, wc);
       if (!ok) break;
     }
-    const long long idx = atomicAdd(a.item_counter, 1);
+    // The first item is the CTA's own index (the grid has at most as many
+    // CTAs as items), so no CTA starts behind a global atomic; later items
+    // come from the counter, past the first gridDim.x.
+    const long long idx = (k == 0) ? static_cast<long long>(blockIdx.x)
+                                   : static_cast<long long>(gridDim.x) + atomicAdd(a.item_counter, 1);
     const BwdItem it = bwd_item_of(idx, a, nkb, nm, kv_items, total);
     sh.items[slot] = it;
     mbar_arrive(&sh.item_full[slot]);  // release: the item is visible to the waiters
