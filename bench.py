@@ -211,6 +211,7 @@ def run_reference(args, w, rank, world):
 
 TRAFFIC_FILES = {
     "fa2_fwd_kernel": ["fa2_fwd.cu", "fa2_common.cuh", "sm103_ptx.cuh"],
+    "fa2_fwd_persist_kernel": ["fa2_fwd.cu", "fa2_fwd_persist.cuh", "fa2_common.cuh", "sm103_ptx.cuh"],
     "fa2_bwd_main_kernel": ["fa2_bwd.cu", "fa2_bwd_persist.cuh", "fa2_bwd_parts.cuh", "fa2_common.cuh",
                             "sm103_ptx.cuh"],
     "fa2_bwd_fused_kernel": ["fa2_bwd_fused.cu", "fa2_bwd_parts.cuh", "fa2_common.cuh",
@@ -533,7 +534,8 @@ def main():
     n_pad = -(-N // 128) * 128
     pre_bytes = B * H * N * (2 * d * 2 + 4 + 8) + (0 if det else B * H * n_pad * d * 4)
     kernels = {
-        ("fa1_order_fwd_kernel" if kv_outer else "fa2_fwd_kernel"): (mean(t_fwd), fw, "tensor"),
+        ("fa1_order_fwd_kernel" if kv_outer else
+         "fa2_fwd_kernel" if fwd_splits > 1 else "fa2_fwd_persist_kernel"): (mean(t_fwd), fw, "tensor"),
         ("fa2_bwd_main_kernel" if det else "fa2_bwd_fused_kernel"): (mean(t_kv), 2.5 * fw, "tensor"),
         "fa2_bwd_pre_kernel": (mean(t_pre), pre_bytes, "hbm"),
     }

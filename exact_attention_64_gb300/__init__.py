@@ -32,6 +32,7 @@ __all__ = [
     "attention",
     "fwd_grid",
     "fwd_block_work",
+    "fwd_schedule",
     "bwd_grid",
     "bwd_block_work",
     "status_string",
@@ -92,6 +93,7 @@ def load_library() -> ctypes.CDLL:
         "fa2_status_string": (ctypes.c_char_p, [i]),
         "fa2_fwd_grid": (i, [i, i, i, _c_int_p, _c_int_p]),
         "fa2_fwd_block_work": (i, [i, i, i, _c_int_p, _c_int_p, _c_int_p]),
+        "fa2_fwd_schedule": (i, [i, i, i, i, i, _c_int_p, _c_int_p, _c_int_p]),
         "fa2_bwd_grid": (i, [i, i, i, i, _c_int_p, _c_int_p, _c_int_p]),
         "fa2_bwd_block_work": (i, [i, i, i, i, _c_int_p, _c_int_p, _c_int_p, _c_int_p]),
         "fa2_debug_arm_fault": (i, [i, i]),
@@ -380,11 +382,25 @@ def fwd_grid(B: int, H: int, N: int):
 
 
 def fwd_block_work(block_x: int, N: int, causal: bool):
-    """(row_begin, row_end, kv_tiles) of forward CTA ``block_x``."""
+    """(row_begin, row_end, kv_tiles) of forward row block ``block_x``."""
     a, b, c = _ints(3)
     _check("fa2_fwd_block_work", load_library().fa2_fwd_block_work(
         block_x, N, int(bool(causal)), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
     return a.value, b.value, c.value
+
+
+def fwd_schedule(B: int, H: int, N: int, causal: bool, num_sms: int):
+    """(num_ctas, cta_of_block, pos_of_block) of the unsplit forward's
+    persistent grid on ``num_sms`` multiprocessors; the lists are in
+    ``fwd_grid`` order (row block fastest, then batch, then head)."""
+    n = load_library()
+    nb = B * H * fwd_grid(1, 1, N)[0][0]
+    g = ctypes.c_int()
+    cta = (ctypes.c_int * nb)()
+    pos = (ctypes.c_int * nb)()
+    _check("fa2_fwd_schedule", n.fa2_fwd_schedule(B, H, N, int(bool(causal)), num_sms,
+                                                  ctypes.byref(g), cta, pos))
+    return g.value, list(cta), list(pos)
 
 
 def bwd_grid(B: int, H: int, N: int, d: int):

@@ -131,13 +131,15 @@ int check_common(int B, int H, int N, int d, int causal, float scale, int dtype)
   return FA2_OK;
 }
 
-// 3-D tensor map over a [B*H][N][d] 16-bit tensor, boxes of 128 rows x 64
-// columns (one 128-byte-swizzled slab), zero fill past row N of each head.
-int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dtype) {
+// 3-D tensor map over a [B*H][N][d] 16-bit tensor, boxes of box_rows rows
+// (128: one tile) x 64 columns (one 128-byte-swizzled slab), zero fill past row
+// N of each head; stores clip there.
+int make_map_16bit(CUtensorMap* m, const void* ptr, int BH, int N, int d, int dtype,
+                   int box_rows = fa2::kTileRows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(fa2::kTileRows), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   const CUresult r =
       g_encode(m, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -218,7 +220,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (st != FA2_OK) return st;
   CUtensorMap tq, tk, tv, to;
   if (make_map_16bit(&tq, q, BH, N, d, dtype) || make_map_16bit(&tk, k, BH, Nk, d, dtype) ||
-      make_map_16bit(&tv, v, BH, Nk, d, dtype) || make_map_16bit(&to, o, BH, N, d, dtype))
+      make_map_16bit(&tv, v, BH, Nk, d, dtype) ||
+      make_map_16bit(&to, o, BH, N, d, dtype, num_splits > 1 ? fa2::kTileRows : 32))
     return FA2_ERR_CUDA;
   fa2::FwdArgs a{};
   a.lse = lse;
@@ -240,6 +243,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.part_done = part_done;
+  a.sched = fa2::fwd_sched_make(BH, a.num_m_blocks, causal, g_num_sms[dev]);
   {
     // An armed failure-path fault is consumed by the next call of its kind:
     // 1 by an unsplit forward, 2 by a split one; both make the producer skip
@@ -658,6 +662,33 @@ int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_
   if (row_begin) *row_begin = r0;
   if (row_end) *row_end = r1;
   if (kv_tiles) *kv_tiles = fa2::fwd_kv_tile_end(r0, r1, N, causal);
+  return FA2_OK;
+}
+
+int fa2_fwd_schedule(int B, int H, int N, int causal, int num_sms, int* num_ctas, int* cta_of_block,
+                     int* pos_of_block) {
+  if (B < 1 || H < 1 || N < 1 || num_sms < 1 || (causal != 0 && causal != 1) || num_ctas == nullptr)
+    return FA2_ERR_INVALID_ARG;
+  const int nm = fa2::fwd_num_m_blocks(N);
+  if (static_cast<long long>(B) * H * nm > (1LL << 31) - 1) return FA2_ERR_UNSUPPORTED;
+  const fa2::FwdSched s = fa2::fwd_sched_make(B * H, nm, causal, num_sms);
+  *num_ctas = s.G;
+  if (cta_of_block == nullptr && pos_of_block == nullptr) return FA2_OK;
+  const long long blocks = static_cast<long long>(B) * H * nm;
+  for (long long i = 0; i < blocks; ++i) {
+    if (cta_of_block) cta_of_block[i] = -1;
+    if (pos_of_block) pos_of_block[i] = -1;
+  }
+  for (int c = 0; c < s.G; ++c) {
+    fa2::FwdCursor cur{};
+    int hb = 0, rank = 0;
+    for (int k = 0; fa2::fwd_sched_next(s, c, cur, &hb, &rank); ++k) {
+      if (hb < 0 || hb >= B * H || rank < 0 || rank >= nm) return FA2_ERR_INVALID_ARG;
+      const long long lin = static_cast<long long>(hb) * nm + rank;
+      if (cta_of_block) cta_of_block[lin] = c;
+      if (pos_of_block) pos_of_block[lin] = k;
+    }
+  }
   return FA2_OK;
 }
 

@@ -68,6 +68,157 @@ __host__ __device__ inline int fwd_block_tiles(int m, int N, int N_k, int causal
   return fwd_kv_tile_end(r0, min(N, r0 + kFwdRowsPerCta), N_k, causal);
 }
 
+// Schedule of the persistent forward: G CTAs (at most one per SM) each run a
+// fixed list of row blocks ("items"). Item (hb, rank) is the row block the
+// per-block grid runs as blockIdx = (rank, hb % B, hb / B), i.e. linear block
+// index hb * nm + rank, and covers rows of block fwd_m_block_of(rank).
+//
+// Without a causal mask every item has the same K/V range: items are dealt
+// round robin (CTA c takes items c, c + G, ...), heads in order, so the CTAs
+// running at any moment share a few heads' K/V through L2.
+//
+// Under a causal mask row block m visits about 2(m + 1) K/V tiles, so ranks q
+// and nm-1-q of a head (blocks nm-1-q and q) form a pair with a constant total.
+// Pairs are dealt round robin, longer block first. The last, partial round
+// would leave most CTAs idle while a few run a whole pair; instead the R
+// leftover pairs are chosen among the most balanced ones (q near the middle,
+// whose two blocks are nearly equal) of the last heads and run as halves, one
+// half per CTA: every CTA then finishes within about half a pair of the mean.
+// Concretely, with P pairs, G = min(P, SMs), R = P mod G, T = ceil(R / BH)
+// middle pairs are reserved in each of the last BHr = ceil(R / T) heads
+// (R' = BHr T >= R of them); the other P - R' = kG - (R' - R) pairs are dealt
+// round robin, which leaves R' - R CTAs one pair short; those run R' - R of the
+// reserved pairs whole, and the other R are split over CTAs 0 .. 2R-1. The
+// reserve is used when nm is even (true pairs), R > 0, T <= pairs per head and
+// R + R' <= G; otherwise the leftover pairs are dealt like the others. When
+// there are at most as many items as SMs, every item gets its own CTA.
+struct FwdSched {
+  int BH, nm;     // heads (batch x heads) and row blocks per head
+  int G;          // CTAs
+  int pairs;      // 0: items round robin; 1: causal pairs
+  int ph;         // pairs per head, ceil(nm / 2) (odd nm: the middle block alone)
+  long long bulk; // pairs dealt round robin
+  int T, BHr;     // reserve: T middle pairs in each of the last BHr heads
+  int Rw, Rs;     // reserved pairs run whole (CTAs G-Rw .. G-1) / as halves (CTAs 0 .. 2Rs-1)
+};
+
+__host__ __device__ inline FwdSched fwd_sched_make(int BH, int nm, int causal, int num_sms) {
+  FwdSched s{};
+  s.BH = BH;
+  s.nm = nm;
+  s.ph = (nm + 1) / 2;
+  const long long items = static_cast<long long>(BH) * nm;
+  if (num_sms < 1) num_sms = 1;
+  if (!causal || items <= num_sms) {
+    s.pairs = 0;
+    s.G = static_cast<int>(items < num_sms ? items : num_sms);
+    return s;
+  }
+  s.pairs = 1;
+  const long long P = static_cast<long long>(BH) * s.ph;
+  s.G = static_cast<int>(P < num_sms ? P : num_sms);
+  s.bulk = P;
+  const long long R = P % s.G;
+  if (nm % 2 == 0 && R > 0) {
+    const long long T = (R + BH - 1) / BH;
+    if (T <= s.ph) {
+      const long long BHr = (R + T - 1) / T;
+      const long long Rp = BHr * T;
+      if (R + Rp <= s.G) {
+        s.T = static_cast<int>(T);
+        s.BHr = static_cast<int>(BHr);
+        s.Rw = static_cast<int>(Rp - R);
+        s.Rs = static_cast<int>(R);
+        s.bulk = P - Rp;
+      }
+    }
+  }
+  return s;
+}
+
+// Position of a CTA in its item list.
+struct FwdCursor {
+  long long j;  // items mode: item round; pairs mode: bulk pair round
+  int half;     // 0 / 1: first / second block of the current pair
+  int stage;    // pairs mode: 0 bulk, 1 reserved pairs, 2 done
+};
+
+// Pair (hb, q) of bulk pair b (heads in order; the reserved heads skip their
+// T middle pairs).
+__host__ __device__ inline void fwd_sched_bulk_pair(const FwdSched& s, long long b, int* hb, int* q) {
+  const long long A = static_cast<long long>(s.BH - s.BHr) * s.ph;
+  if (b < A) {
+    *hb = static_cast<int>(b / s.ph);
+    *q = static_cast<int>(b % s.ph);
+  } else {
+    const int w = s.ph - s.T;
+    *hb = s.BH - s.BHr + static_cast<int>((b - A) / w);
+    *q = static_cast<int>((b - A) % w);
+  }
+}
+
+// Reserved pair r: head BH - BHr + r / T, pair ph - 1 - r % T.
+__host__ __device__ inline void fwd_sched_reserved_pair(const FwdSched& s, int r, int* hb, int* q) {
+  *hb = s.BH - s.BHr + r / s.T;
+  *q = s.ph - 1 - r % s.T;
+}
+
+// Next item of CTA c: writes its head index hb and rank and advances the
+// cursor; returns false when the CTA's list is exhausted.
+__host__ __device__ inline bool fwd_sched_next(const FwdSched& s, int c, FwdCursor& cur, int* hb,
+                                               int* rank) {
+  const int nm = s.nm;
+  if (!s.pairs) {
+    const long long u = c + cur.j * s.G;
+    if (u >= static_cast<long long>(s.BH) * nm) return false;
+    ++cur.j;
+    *hb = static_cast<int>(u / nm);
+    *rank = static_cast<int>(u % nm);
+    return true;
+  }
+  for (;;) {
+    int q;
+    if (cur.stage == 0) {
+      const long long b = c + cur.j * s.G;
+      if (b >= s.bulk) {
+        cur.stage = 1;
+        cur.half = 0;
+        continue;
+      }
+      fwd_sched_bulk_pair(s, b, hb, &q);
+    } else if (cur.stage == 1) {
+      if (c >= s.G - s.Rw) {  // a reserved pair run whole
+        fwd_sched_reserved_pair(s, c - (s.G - s.Rw), hb, &q);
+      } else if (c < 2 * s.Rs) {  // half of a reserved pair
+        if (cur.half > 0) return false;
+        fwd_sched_reserved_pair(s, s.Rw + c / 2, hb, &q);
+        cur.half = 1;
+        cur.stage = 2;
+        *rank = (c % 2 == 0) ? q : nm - 1 - q;
+        return true;
+      } else {
+        return false;
+      }
+    } else {
+      return false;
+    }
+    // A pair: rank q, then rank nm-1-q (none when they coincide).
+    if (cur.half == 0) {
+      cur.half = 1;
+      if (nm - 1 - q == q) {
+        cur.half = 0;
+        if (cur.stage == 0) ++cur.j; else cur.stage = 2;
+      }
+      *rank = q;
+      return true;
+    }
+    cur.half = 0;
+    if (cur.stage == 0) ++cur.j; else cur.stage = 2;
+    *rank = nm - 1 - q;
+    return true;
+  }
+}
+
 // Backward work mapping. dK and dV accumulate along the query direction, so
 // their worker owns a K/V column block ("FlashAttention学习笔记(2)",
 // Foward和backward中的thread block划分): one CTA per 128-key block, the column
@@ -96,12 +247,14 @@ struct FwdArgs {
   int num_m_blocks;   // ceil(N / 256)
   float scale_log2;   // scale * log2(e)
   int* status;        // device status word
-  int* tile_count;    // optional: per-CTA count of K/V tiles loaded (nullptr = off)
+  int* tile_count;    // optional: K/V tiles loaded per row block, in per-block grid order (nullptr = off)
   unsigned long long timeout_ns;  // bound on every mbarrier wait
-  int fault;          // 0 normally; 1 = producer skips the first V tile (failure-path test)
+  int fault;          // 0 normally; 1 = the first V tile (of the first CTA, unsplit) never loads (failure-path test)
   int num_splits;     // K/V parts of the longest worker; <= 1: no split
   int kv_tiles_max;   // split mode: K/V tile count of the longest row block
-  void* o;            // split mode: [B*H][N][d] 16-bit output, written by the merging group
+  FwdSched sched;     // unsplit: the persistent kernel's item lists
+  void* o;            // [B*H][N][d] 16-bit output (unsplit: the persistent kernel's row stores;
+                      // split: written by the merging group)
   float* o_part;      // split mode: [num_splits][B*H][N][d] fp32 O / l of each part
   float* lse_part;    // split mode: [num_splits][B*H][N] fp32 logsumexp of each part (-inf: empty)
   int* part_done;     // split mode: [B*H][num_m_blocks][2] arrivals per row tile, zero on entry

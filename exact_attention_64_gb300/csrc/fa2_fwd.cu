@@ -207,6 +207,99 @@ __device__ __forceinline__ void tma_load_tile(uint8_t* dst, const CUtensorMap* m
     tma_load_3d(dst + s * FwdCfg<D>::SLAB_BYTES, map, bar, s * 64, row, bh);
 }
 
+// One K/V step of a softmax warp, for its row my_row of tile t: S from TMEM,
+// the mask, the row max, the lazy rescale of O (exact: O and l share the
+// reference max), P into TMEM over the upper half of S, and the arrival on
+// p_full. s_par is this step's s_full parity, o_prev_par the previous step's
+// o_full parity; first marks the tile's first step. Returns false if a wait
+// gave up.
+template <int D, bool BF16, bool CAUSAL>
+__device__ __forceinline__ bool fwd_softmax_step(uint64_t* s_full, uint64_t* o_full, uint64_t* p_full,
+                                                 uint32_t t_s, uint32_t t_p, uint32_t t_o, int kv0,
+                                                 int row_base, int my_row, int Nk, float sl2, bool first,
+                                                 uint32_t s_par, uint32_t o_prev_par, float& m_ref,
+                                                 float& l, int lane, const WaitCtx& wc) {
+  bool ok = mbar_wait_warp(s_full, s_par, wc);
+  if (!ok) return false;
+  __syncwarp();  // the warp-collective TMEM loads below need a converged warp
+  tc_fence_after();
+  uint32_t s[128];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    tmem_ld_32x32b_x32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
+  tmem_wait_ld();
+  reg_fence(s);
+  // Mask keys past the sequence end and, on the diagonal tile, keys after the query.
+  const bool need_mask = (kv0 + kTileRows > Nk) || (CAUSAL && kv0 + kTileRows - 1 > row_base);
+  if (need_mask) {
+    const int lim = CAUSAL ? min(Nk - kv0, my_row - kv0 + 1) : (Nk - kv0);
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c >= lim) s[c] = __float_as_uint(-INFINITY);
+  }
+  // Row max as eight independent chains of three-input maxima (short
+  // dependency chains, half the instructions of two-input maxima).
+  float mx8[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(__uint_as_float(s[u]), __uint_as_float(s[8 + u]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16)
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      mx8[u] = fmax3(mx8[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
+  const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
+                         fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
+  const float m_new = fmaxf(m_ref, mx);
+  const bool rescale = (m_new - m_ref) * sl2 > kRescaleLog2;  // also true when m_ref = -inf
+  float alpha = 1.f;
+  if (rescale) {
+    alpha = ex2_approx((m_ref - m_new) * sl2);
+    m_ref = m_new;
+  }
+  const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * sl2;
+  // Packed fp32 pairs (f32x2) for the exponent arguments and the row-sum
+  // partials: half the FMA-pipe instructions of the scalar form, same
+  // results. rs[k] accumulates columns 8u+2k and 8u+2k+1.
+  float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                  make_float2(0.f, 0.f)};
+  const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
+#pragma unroll
+  for (int c = 0; c < 64; ++c) {
+    const float2 x = f2_fma(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
+                            sl2x2, negx2);
+    const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    rs[c & 3] = f2_add(rs[c & 3], p);
+    s[c] = pack_x2<BF16>(p.x, p.y);
+  }
+  l = l * alpha + (((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) +
+                   ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y)));
+  tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+  tmem_st_32x32b_x32(t_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+  tmem_wait_st();
+  if (!first && __any_sync(0xffffffffu, rescale)) {
+    // O_t still holds the sum up to the previous step: wait for that product, then rescale.
+    ok = mbar_wait_warp(o_full, o_prev_par, wc);
+    if (!ok) return false;
+    __syncwarp();
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t o[32];
+      tmem_ld_32x32b_x32(t_o + c, o);
+      tmem_wait_ld();
+      reg_fence(o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+      tmem_st_32x32b_x32(t_o + c, o);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(p_full);
+  return true;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(384, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -393,85 +486,10 @@ __global__ void __launch_bounds__(384, 1)
     float l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      ok = mbar_wait_warp(&sh.s_full[t], j & 1, wc);
+      ok = fwd_softmax_step<D, BF16, CAUSAL>(&sh.s_full[t], &sh.o_full[t], &sh.p_full[t], t_s, t_p, t_o,
+                                             (kv_lo + j) * kTileRows, row_base, my_row, Nk, sl2, j == 0,
+                                             j & 1, (j - 1) & 1, m_ref, l, lane, wc);
       if (!ok) break;
-      __syncwarp();  // the warp-collective TMEM loads below need a converged warp
-      tc_fence_after();
-      uint32_t s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld_32x32b_x32(t_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&s[32 * c]));
-      tmem_wait_ld();
-      reg_fence(s);
-      // Mask keys past the sequence end and, on the diagonal tile, keys after the query.
-      const int kv0 = (kv_lo + j) * kTileRows;
-      const bool need_mask = (kv0 + kTileRows > Nk) || (CAUSAL && kv0 + kTileRows - 1 > row_base);
-      if (need_mask) {
-        const int lim = CAUSAL ? min(Nk - kv0, my_row - kv0 + 1) : (Nk - kv0);
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) s[c] = __float_as_uint(-INFINITY);
-      }
-      // Row max as eight independent chains of three-input maxima (short
-      // dependency chains, half the instructions of two-input maxima).
-      float mx8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = fmaxf(__uint_as_float(s[u]), __uint_as_float(s[8 + u]));
-#pragma unroll
-      for (int c = 16; c < 128; c += 16)
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          mx8[u] = fmax3(mx8[u], __uint_as_float(s[c + u]), __uint_as_float(s[c + 8 + u]));
-      const float mx = fmaxf(fmax3(mx8[0], mx8[1], mx8[2]),
-                             fmax3(fmax3(mx8[3], mx8[4], mx8[5]), mx8[6], mx8[7]));
-      const float m_new = fmaxf(m_ref, mx);
-      const bool rescale = (m_new - m_ref) * sl2 > kRescaleLog2;  // also true when m_ref = -inf
-      float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2_approx((m_ref - m_new) * sl2);
-        m_ref = m_new;
-      }
-      const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref * sl2;
-      // Packed fp32 pairs (f32x2) for the exponent arguments and the row-sum
-      // partials: half the FMA-pipe instructions of the scalar form, same
-      // results. rs[k] accumulates columns 8u+2k and 8u+2k+1.
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
-      const float2 sl2x2 = make_float2(sl2, sl2), negx2 = make_float2(neg, neg);
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float2 x = f2_fma(make_float2(__uint_as_float(s[2 * c]), __uint_as_float(s[2 * c + 1])),
-                                sl2x2, negx2);
-        const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        rs[c & 3] = f2_add(rs[c & 3], p);
-        s[c] = pack_x2<BF16>(p.x, p.y);
-      }
-      l = l * alpha + (((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) +
-                       ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y)));
-      tmem_st_32x32b_x32(t_p, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_st_32x32b_x32(t_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_wait_st();
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O_t still holds the sum up to tile j-1: wait for that product, then rescale.
-        ok = mbar_wait_warp(&sh.o_full[t], (j - 1) & 1, wc);
-        if (!ok) break;
-        __syncwarp();
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(t_o + c, o);
-          tmem_wait_ld();
-          reg_fence(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st_32x32b_x32(t_o + c, o);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.p_full[t]);
     }
     // ---------------- epilogue: O / l -> 16-bit, L = m + ln l ----------------
     if (ok && nt > 0) ok = mbar_wait_warp(&sh.o_full[t], (nt - 1) & 1, wc);
@@ -571,25 +589,39 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+}  // namespace fa2
+
+#include "fa2_fwd_persist.cuh"
+
+namespace fa2 {
+
 // ---------------------------------------------------------------------------
-// Host-side launcher (called by the C ABI after validation).
+// Host-side launcher (called by the C ABI after validation). Without a K/V
+// split the persistent kernel runs the row blocks (a.sched: at most one CTA
+// per SM; `to` has 32-row boxes, one softmax warp's rows); with one, the
+// per-block kernel runs one CTA per (row block, part) (`to`: 128-row boxes).
 // ---------------------------------------------------------------------------
 template <int D, bool BF16, bool CAUSAL>
 static cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                 const CUtensorMap& to, const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
+  if (a.num_splits <= 1) {
+    auto pk = fa2_fwd_persist_kernel<D, BF16, CAUSAL>;
+    constexpr int smem = FwdPCfg<D>::SMEM_ALLOC;
+    cudaError_t e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (a.sched.G < 1) return cudaErrorInvalidConfiguration;
+    pk<<<a.sched.G, C::THREADS, smem, stream>>>(tq, tk, tv, to, a);
+    return cudaGetLastError();
+  }
   auto kern = fa2_fwd_kernel<D, BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_m_blocks, a.B, a.H);
-  if (a.num_splits > 1) {
-    const long long ctas = split_ctas(a.num_m_blocks, a.num_splits, a.kv_tiles_max, a.B * a.H, [&](int k) {
-      return fwd_block_tiles(fwd_m_block_of(k, a.num_m_blocks, CAUSAL), a.N, a.Nk, CAUSAL);
-    });
-    if (ctas < 1 || ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    grid = dim3(static_cast<unsigned>(ctas), 1, 1);
-  }
-  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
+  const long long ctas = split_ctas(a.num_m_blocks, a.num_splits, a.kv_tiles_max, a.B * a.H, [&](int k) {
+    return fwd_block_tiles(fwd_m_block_of(k, a.num_m_blocks, CAUSAL), a.N, a.Nk, CAUSAL);
+  });
+  if (ctas < 1 || ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<static_cast<unsigned>(ctas), C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 

@@ -287,16 +287,30 @@ int fa2_get_device_status(void* stream);
 const char* fa2_status_string(int status);
 
 /* ---- Host-only queries of the work mapping (no GPU needed) ----------------
- * Forward grid = (num_m_block, B, H), the row block varying fastest
- * ("FlashAttention学习笔记(2)", V2中的thread blocks排布). Each CTA owns
- * rows_per_cta = 256 query rows (two 128-row tiles). */
+ * Forward row blocks ("thread blocks" of "FlashAttention学习笔记(2)",
+ * V2中的thread blocks排布) form the grid (num_m_block, B, H), the row block
+ * varying fastest. Each owns rows_per_cta = 256 query rows (two 128-row
+ * tiles). The split forward launches one CTA per (row block, part); the
+ * unsplit one runs the row blocks on a persistent grid (fa2_fwd_schedule). */
 int fa2_fwd_grid(int B, int H, int N, int grid_out[3], int* rows_per_cta);
 
 /* Query rows [*row_begin, *row_end) and the number of K/V tiles of 128 keys
- * that forward CTA `block_x` loads (causal: fully masked tiles are skipped,
- * "flash-attention123和ring-attention", 优化3). */
+ * that forward row block `block_x` loads (causal: fully masked tiles are
+ * skipped, "flash-attention123和ring-attention", 优化3). */
 int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_end,
                        int* kv_tiles);
+
+/* Schedule of the unsplit forward on a device with num_sms multiprocessors:
+ * *num_ctas CTAs (at most num_sms), each running a fixed list of row blocks.
+ * Without a causal mask the row blocks are dealt round robin; with one, pairs
+ * of row blocks q and num_m_block-1-q (a constant K/V total) are dealt round
+ * robin, and the pairs left for a last partial round are the most balanced
+ * ones of the last heads, run as halves. cta_of_block and pos_of_block (host
+ * arrays of B*H*num_m_block ints, in fa2_fwd_grid order; either may be NULL)
+ * receive each row block's CTA and its position in that CTA's list.
+ * Returns FA2_ERR_INVALID_ARG for sizes < 1, causal not 0/1 or a NULL num_ctas. */
+int fa2_fwd_schedule(int B, int H, int N, int causal, int num_sms, int* num_ctas, int* cta_of_block,
+                     int* pos_of_block);
 
 /* Backward dK/dV grid = (num_n_block, B, H): one CTA per 128-key column block
  * ("FlashAttention学习笔记(2)", Foward和backward中的thread block划分). */
@@ -309,9 +323,9 @@ int fa2_bwd_block_work(int block_x, int N, int d, int causal, int* key_begin, in
                        int* q_tile_begin, int* q_tile_end);
 
 /* ---- Diagnostics ----------------------------------------------------------
- * fa2_fwd, plus: tile_counts (device int array with one slot per forward CTA,
- * grid order x fastest, or NULL) receives the number of K/V tiles each CTA
- * actually loaded. */
+ * fa2_fwd, plus: tile_counts (device int array with one slot per forward row block,
+ * grid order x fastest, or NULL) receives the number of K/V tiles loaded for
+ * each row block. */
 int fa2_fwd_instrumented(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int N, int d, int causal, float scale, int dtype, int* tile_counts,
                          void* stream);
