@@ -445,11 +445,15 @@ __device__ bool bwd_persist_compute(BwdPShared& sh, uint8_t* smem, uint32_t tmem
         const int g = n.kv_tiles + i;
         const int q0 = (i_begin + i) * kTileRows;
         const int qc0 = q0 + 64 * wg;  // first query column of this warpgroup
-        {
-          // Coalesced loads (they do not depend on S) before waiting for the scores.
-          const size_t row = static_cast<size_t>(bh) * a.n_pad + qc0 + 2 * lane;
-          const float2 l2v = *reinterpret_cast<const float2*>(a.l2_pad + row);
-          const float2 dv2 = *reinterpret_cast<const float2*>(a.dsum_pad + row);
+        // L * log2e and D of this warpgroup's 64 query columns, the same for
+        // every thread, loaded before waiting for the scores (they do not
+        // depend on S). At d = 128 the warp stages them through its shared
+        // slice (coalesced loads, then broadcast reads); at d = 64 warp-uniform
+        // 16-byte loads through L1 measured faster (and slower at d = 128).
+        const size_t crow = static_cast<size_t>(bh) * a.n_pad + qc0;
+        if (D != 64) {
+          const float2 l2v = *reinterpret_cast<const float2*>(a.l2_pad + crow + 2 * lane);
+          const float2 dv2 = *reinterpret_cast<const float2*>(a.dsum_pad + crow + 2 * lane);
           __syncwarp();  // every lane is done with the previous step's values
           *reinterpret_cast<float2*>(ld_s + 2 * lane) = make_float2(-l2v.x, -l2v.y);
           *reinterpret_cast<float2*>(ld_s + 64 + 2 * lane) = dv2;
@@ -458,7 +462,13 @@ __device__ bool bwd_persist_compute(BwdPShared& sh, uint8_t* smem, uint32_t tmem
         float lreg[64];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float4 l4 = reinterpret_cast<const float4*>(ld_s)[u];
+          float4 l4;
+          if (D == 64) {
+            l4 = __ldg(reinterpret_cast<const float4*>(a.l2_pad + crow) + u);
+            l4 = make_float4(-l4.x, -l4.y, -l4.z, -l4.w);
+          } else {
+            l4 = reinterpret_cast<const float4*>(ld_s)[u];
+          }
           lreg[4 * u] = l4.x; lreg[4 * u + 1] = l4.y; lreg[4 * u + 2] = l4.z; lreg[4 * u + 3] = l4.w;
         }
         ok = mbar_wait_warp(&sh.st_full, g & 1, wc);
@@ -492,7 +502,8 @@ __device__ bool bwd_persist_compute(BwdPShared& sh, uint8_t* smem, uint32_t tmem
         float dreg[64];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float4 d4 = reinterpret_cast<const float4*>(ld_s + 64)[u];
+          const float4 d4 = D == 64 ? __ldg(reinterpret_cast<const float4*>(a.dsum_pad + crow) + u)
+                                    : reinterpret_cast<const float4*>(ld_s + 64)[u];
           dreg[4 * u] = d4.x; dreg[4 * u + 1] = d4.y; dreg[4 * u + 2] = d4.z; dreg[4 * u + 3] = d4.w;
         }
         ok = mbar_wait_warp(&sh.dpt_full, g & 1, wc);
