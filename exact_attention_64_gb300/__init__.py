@@ -413,7 +413,7 @@ def bwd_grid(B: int, H: int, N: int, d: int):
 
 
 def bwd_block_work(block_x: int, N: int, d: int, causal: bool):
-    """(key_begin, key_end, q_tile_begin, q_tile_end) of dK/dV CTA ``block_x``."""
+    """(key_begin, key_end, q_tile_begin, q_tile_end) of dK/dV column block ``block_x``."""
     a, b, c, e = _ints(4)
     _check("fa2_bwd_block_work", load_library().fa2_bwd_block_work(
         block_x, N, d, int(bool(causal)), ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),

@@ -312,13 +312,15 @@ int fa2_fwd_block_work(int block_x, int N, int causal, int* row_begin, int* row_
 int fa2_fwd_schedule(int B, int H, int N, int causal, int num_sms, int* num_ctas, int* cta_of_block,
                      int* pos_of_block);
 
-/* Backward dK/dV grid = (num_n_block, B, H): one CTA per 128-key column block
- * ("FlashAttention学习笔记(2)", Foward和backward中的thread block划分). */
+/* Backward dK/dV work = (num_n_block, B, H): one worker per 128-key column
+ * block ("FlashAttention学习笔记(2)", Foward和backward中的thread block划分). The
+ * main launch runs these workers, then the dQ workers, on a persistent grid
+ * of at most one CTA per SM. */
 int fa2_bwd_grid(int B, int H, int N, int d, int grid_out[3], int* keys_per_cta,
                  int* q_rows_per_tile);
 
-/* Keys [*key_begin, *key_end) of backward CTA `block_x` and the query tiles
- * [*q_tile_begin, *q_tile_end) (of q_rows_per_tile rows) it visits. */
+/* Keys [*key_begin, *key_end) of backward column block `block_x` and the query
+ * tiles [*q_tile_begin, *q_tile_end) (of q_rows_per_tile rows) it visits. */
 int fa2_bwd_block_work(int block_x, int N, int d, int causal, int* key_begin, int* key_end,
                        int* q_tile_begin, int* q_tile_end);
 
