@@ -45,7 +45,7 @@ def parse():
     p.add_argument("--impl", default="fa2", choices=["fa2", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--cpu-sample-heads", type=int, default=3)
+    p.add_argument("--cpu-sample-heads", type=int, default=6)
     p.add_argument("--no-configs", action="store_true",
                    help="skip the forward/backward lines of the other configurations")
     p.add_argument("--fwd-splits", default="auto",
