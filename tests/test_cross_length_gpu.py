@@ -23,6 +23,9 @@ CASES = [
     (1, 1, 200, 640, 128, torch.bfloat16, True),
     (1, 3, 1000, 333, 64, torch.float16, False),
     (1, 1, 129, 1000, 128, torch.float16, False),
+    # 80 heads x 4 row blocks: the persistent forward runs causal pairs (160 of
+    # them on 152 CTAs, the last 8 as halves) with N_k < N_q.
+    (4, 20, 1024, 600, 64, torch.bfloat16, True),
 ]
 
 

@@ -100,19 +100,22 @@ def test_fwd_headline_eight_seeded_heads(cuda_device, fa2_lib):
         assert max_abs(l64[b, h], lse_ref[0, 0]) <= tol["lse"], (b, h)
 
 
-def test_fwd_causal_tiles_skipped(cuda_device, fa2_lib):
-    """Each CTA loads exactly the K/V tiles up to the diagonal, none past it."""
-    B, H, N, d = 1, 2, 1000, 128
+@pytest.mark.parametrize("B,H,N", [(1, 2, 1000), (4, 15, 1380)])
+def test_fwd_causal_tiles_skipped(cuda_device, fa2_lib, B, H, N):
+    """Each row block loads exactly the K/V tiles up to the diagonal, none past
+    it. The second shape has 360 row blocks, so the persistent grid runs several
+    per CTA (causal: pairs, and a last round of halves)."""
+    d = 128
     q, k, v, _ = make_inputs(B, H, N, d, torch.bfloat16, seed=3)
     dev = cuda_device
     for causal in (False, True):
         _, _, counts = fa2_lib.forward_instrumented(q.to(dev), k.to(dev), v.to(dev), causal=causal)
         counts = counts.cpu().numpy()
         (gx, gy, gz), _ = fa2_lib.fwd_grid(B, H, N)
-        for cta in range(gx * gy * gz):
-            bx = cta % gx
+        for blk in range(gx * gy * gz):
+            bx = blk % gx
             _, _, want = fa2_lib.fwd_block_work(bx, N, causal)
-            assert counts[cta] == want, (causal, cta)
+            assert counts[blk] == want, (causal, blk)
 
 
 def test_fwd_device_timeout_path(cuda_device, fa2_lib):
